@@ -1,0 +1,174 @@
+/*
+ * Plain CPU oracle of C = relu(A·B) for fp16 A (M,K), B (K,N), row-major.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline
+ * leg may load this library.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes (TileLang paper-reading page, section 2, the matmul_relu example):
+ *   the accumulator fragment is float32 and starts cleared (T.clear); every k-step adds
+ *   A_tile·B_tile into it (T.gemm); the epilogue replaces each element x by max(x, 0)
+ *   (the T.Parallel loop with T.max) and the copy to the float16 C rounds it.
+ * The practitioner page (section 3.2) states why the accumulator is float32 and not float16.
+ *
+ * So, element by element,
+ *     C[i,j] = fp16_rne( relu( sum_{k=0}^{K-1} A[i,k]*B[k,j] ) )
+ * with the sum formed in float32 in increasing k.  Every fp16*fp16 product has at most 22
+ * significant bits and an exponent inside float32's range, so each product is exact in
+ * float32 and the only roundings are the K-1 additions (FMA contraction cannot change the
+ * result).  A second accumulator in float64 (same order) gives the near-exact reference
+ * that the tolerance is measured against; it is rounded to fp16 directly, once.
+ *
+ * relu(x) = (x > 0) ? x : +0, so -0 and NaN give +0.  fp16 rounding: IEEE 754 binary16,
+ * round to nearest with ties to even, subnormals kept, overflow to infinity.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- IEEE 754 binary16 encode / decode, written from the format's definition ---- */
+
+/* Round a non-negative double q (< 2^53) to the nearest integer, ties to even. */
+static double round_half_even(double q) {
+  double fl = floor(q);
+  double diff = q - fl; /* exact: q and fl share exponent range */
+  if (diff > 0.5) return fl + 1.0;
+  if (diff < 0.5) return fl;
+  return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* binary64 -> binary16 bits, round to nearest even. NaN -> quiet NaN 0x7E00 with the sign. */
+uint16_t tg_oracle_f64_to_f16(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+  double a = fabs(x);
+  /* largest finite is 65504 = (2 - 2^-10) * 2^15; the midpoint to 2^16 is 65520 and the tie
+     goes to the even neighbour 2^16, which overflows: so a >= 65520 -> infinity. */
+  if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);
+  if (a < 0x1p-14) {
+    /* subnormal range: value = m * 2^-24 with m in [0, 1024]; m == 1024 is the smallest normal
+       and its bit pattern 0x0400 follows on directly. */
+    double m = round_half_even(ldexp(a, 24));
+    return (uint16_t)(sign | (uint16_t)m);
+  }
+  int e2;
+  double fr = frexp(a, &e2);         /* a = fr * 2^e2, fr in [0.5, 1) */
+  int e = e2 - 1;                    /* a = s * 2^e, s in [1, 2), e in [-14, 15] */
+  double q = ldexp(fr, 11);          /* s * 2^10 in [1024, 2048), exact */
+  double r = round_half_even(q);
+  if (r == 2048.0) { r = 1024.0; e += 1; }
+  if (e > 15) return (uint16_t)(sign | 0x7C00u);
+  return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(r - 1024.0));
+}
+
+/* binary32 -> binary16: every float is exactly a double, so this is the same rounding. */
+uint16_t tg_oracle_f32_to_f16(float x) { return tg_oracle_f64_to_f16((double)x); }
+
+/* binary16 bits -> exact double value. */
+double tg_oracle_f16_to_f64(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int ex = (h >> 10) & 0x1F;
+  int man = h & 0x3FF;
+  double v;
+  if (ex == 0x1F) {
+    v = man ? NAN : INFINITY;
+  } else if (ex == 0) {
+    v = ldexp((double)man, -24);
+  } else {
+    v = ldexp((double)(1024 + man), ex - 25);
+  }
+  return sign ? -v : v;
+}
+
+void tg_oracle_f32_to_f16_array(const float* x, uint16_t* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = tg_oracle_f32_to_f16(x[i]);
+}
+void tg_oracle_f64_to_f16_array(const double* x, uint16_t* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = tg_oracle_f64_to_f16(x[i]);
+}
+void tg_oracle_f16_to_f64_array(const uint16_t* x, double* y, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) y[i] = tg_oracle_f16_to_f64(x[i]);
+}
+
+static float relu32(float x) { return (x > 0.0f) ? x : 0.0f; }
+static double relu64(double x) { return (x > 0.0) ? x : 0.0; }
+
+/*
+ * relu(A·B) on a sub-grid of C: rows rows[0..nr-1] and columns cols[0..nc-1] (nr*nc outputs,
+ * row-major in the outputs).  With every row and column selected this is the whole C.
+ *
+ *   out16_f32acc[r*nc+c]  fp16 bits of relu(float32 sum)          (may be NULL)
+ *   acc_f32[r*nc+c]       float32 sum before relu                  (may be NULL)
+ *   out16_f64acc[r*nc+c]  fp16 bits of relu(float64 sum)          (may be NULL)
+ *   acc_f64[r*nc+c]       float64 sum before relu                  (may be NULL)
+ *   relu                  1: apply relu; 0: identity epilogue
+ *   nthreads              OpenMP threads over rows (0 = runtime default)
+ *
+ * Returns 0, or -1 on a bad argument or allocation failure.
+ */
+int tg_oracle_gemm_relu(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, const int64_t* rows, int64_t nr,
+                        const int64_t* cols, int64_t nc, int relu, uint16_t* out16_f32acc,
+                        float* acc_f32, uint16_t* out16_f64acc, double* acc_f64, int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || nr < 0 || nc < 0) return -1;
+  if (K > 0 && (lda < K || ldb < N)) return -1;
+  for (int64_t r = 0; r < nr; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return -1;
+  for (int64_t c = 0; c < nc; ++c)
+    if (cols[c] < 0 || cols[c] >= N) return -1;
+  if (nr == 0 || nc == 0) return 0;
+  const int want32 = (out16_f32acc != NULL) || (acc_f32 != NULL);
+  const int want64 = (out16_f64acc != NULL) || (acc_f64 != NULL);
+
+  /* decode the selected columns of B once: Bsel[k*nc + c] = B[k, cols[c]] (exact) */
+  float* Bsel = (float*)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1) * (size_t)nc);
+  if (!Bsel) return -1;
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t c = 0; c < nc; ++c)
+      Bsel[k * nc + c] = (float)tg_oracle_f16_to_f64(B[k * ldb + cols[c]]);
+
+  int failed = 0;
+#ifdef _OPENMP
+  int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+#endif
+  for (int64_t r = 0; r < nr; ++r) {
+    float* s32 = (float*)calloc((size_t)nc, sizeof(float));
+    double* s64 = (double*)calloc((size_t)nc, sizeof(double));
+    if (!s32 || !s64) {
+      failed = 1;
+    } else {
+      const uint16_t* arow = A + rows[r] * lda;
+      for (int64_t k = 0; k < K; ++k) {
+        float a = (float)tg_oracle_f16_to_f64(arow[k]);
+        const float* brow = Bsel + k * nc;
+        if (want32)
+          for (int64_t c = 0; c < nc; ++c) s32[c] = s32[c] + a * brow[c];
+        if (want64)
+          for (int64_t c = 0; c < nc; ++c) s64[c] = s64[c] + (double)a * (double)brow[c];
+      }
+      for (int64_t c = 0; c < nc; ++c) {
+        int64_t o = r * nc + c;
+        if (acc_f32) acc_f32[o] = s32[c];
+        if (out16_f32acc) out16_f32acc[o] = tg_oracle_f32_to_f16(relu ? relu32(s32[c]) : s32[c]);
+        if (acc_f64) acc_f64[o] = s64[c];
+        if (out16_f64acc) out16_f64acc[o] = tg_oracle_f64_to_f16(relu ? relu64(s64[c]) : s64[c]);
+      }
+    }
+    free(s32);
+    free(s64);
+  }
+  free(Bsel);
+  return failed ? -1 : 0;
+}
+
+int tg_oracle_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
