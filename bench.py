@@ -1,0 +1,410 @@
+"""Benchmark of relu(A·B) on GB300: GEMM+ReLU TFLOP/s (2MNK / device time) and the fraction of
+the GB300 roofline, for one named workload (default: the 8192^3 compute-bound case).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the C ABI (tg_gemm_relu_f16) on inputs already resident in HBM.
+Prints ONE JSON line on rank 0.  Under torchrun each rank runs an independent replica on its
+own GPU (the path needs no exchange between GPUs); ``value`` is the work of all ranks over the
+slowest rank's time.  ``--impl reference`` times the CPU oracle instead (host cores only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from fp16_gemm_relu_gb300 import workloads  # noqa: E402
+
+METRIC = "GEMM+ReLU TFLOP/s (2MNK/t) and % of GB300 fp16 tensor/HBM roofline, 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP16_OVER_BF16 = 1.0  # dense fp16 and bf16 tensor rates are equal (nominal 2.25 PF each)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="square8192", choices=workloads.ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target seconds of oracle work for the cpu_baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "fp16_gemm_relu_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it was
+    taken on the current kernel source (its 'source_hash' line must match)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == workload and parts[1] == cur:
+            return float(parts[2])
+    return None
+
+
+# ----------------------------------- clocks -----------------------------------
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons of one GPU while running, through NVML
+    (read-only queries), falling back to nvidia-smi."""
+
+    REASONS = {0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []  # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._smi = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle for " + pci_bus_id)
+            self._nvml, self._handle = nv, h
+            v = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(v)) == 0:  # NVML_CLOCK_SM
+                self.max_mhz = float(v.value)
+        except OSError:
+            self._nvml = None
+        self.pci = pci_bus_id
+
+    def _poll_nvml(self):
+        nv, h = self._nvml, self._handle
+        clk = ctypes.c_uint()
+        reasons = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = 0
+                if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(reasons)) == 0:
+                    r = reasons.value
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll_nvml, daemon=True)
+            self._thread.start()
+        else:
+            q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.pci}", f"--query-gpu={q}",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self._smi = None
+
+    def stop(self):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+        if self._smi is not None:
+            self._smi.terminate()
+            out, _ = self._smi.communicate(timeout=10)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    sm, mx = float(f[0]), float(f[1])
+                except ValueError:
+                    continue
+                self.max_mhz = mx
+                mask = 0
+                for i, n in enumerate(names):
+                    if f[2 + i].lower().startswith("active"):
+                        mask |= {v: k for k, v in self.REASONS.items()}[n]
+                self.samples.append((sm, mask))
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = sorted(n for bit, n in self.REASONS.items() if mask & bit)
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+
+
+# ----------------------------------- helpers -----------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_baseline(wl, a, b, target_s: float, relu=True):
+    """The oracle as it stands, on a bounded sample: the first R rows of C."""
+    import oracle
+
+    dt, flops, threads = oracle.timed_rows(a, b, 2, relu=relu)  # calibration
+    per_row = dt / 2
+    rows = int(max(1, min(wl.M, target_s / max(per_row, 1e-6))))
+    dt, flops, threads = oracle.timed_rows(a, b, rows, relu=relu)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} of {wl.M} rows of C ({rows}x{wl.N}x{wl.K}), float32 "
+                      f"accumulation, {dt:.1f} s"}
+
+
+def run_reference(args, wl):
+    """The oracle on the host cores: each step computes a bounded sample of C's rows."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+
+    a, b = wl.make_a(), wl.make_b()
+    steps, warm = max(args.steps, 1), max(args.warmup, 0)
+    budget = 150.0 / (steps + warm)  # the whole run within a few minutes
+    dt, _, _ = oracle.timed_rows(a, b, 1)
+    rows = int(max(1, min(wl.M, budget / max(dt, 1e-6))))
+    for _ in range(warm):
+        oracle.timed_rows(a, b, rows)
+    times = []
+    flops = 0.0
+    threads = oracle.max_threads()
+    for _ in range(steps):
+        t, f, threads = oracle.timed_rows(a, b, rows)
+        times.append(t)
+        flops += f
+    total = sum(times)
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": steps, "warmup": warm, "ms_per_step": 1e3 * total / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 inputs of the workload's distribution)",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"first {rows} rows of C per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+
+    import fp16_gemm_relu_gb300 as tg
+    from fp16_gemm_relu_gb300 import binding, build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    binding.load_library()
+
+    a_np, b_np = wl.make_a(), wl.make_b()
+    props = torch.cuda.get_device_properties(dev)
+    A_h = torch.from_numpy(a_np).pin_memory()
+    B_h = torch.from_numpy(b_np).pin_memory()
+    A = A_h.to(dev)
+    B = B_h.to(dev)
+    C = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+    plan = tg.plan(wl.M, wl.N, wl.K, num_sms=props.multi_processor_count,
+                   a_ptr=A.data_ptr(), b_ptr=B.data_ptr(), c_ptr=C.data_ptr())
+    in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2
+    flush = in_bytes <= L2_BYTES
+    scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
+
+    stream = torch.cuda.Stream(dev)
+    handle = stream.cuda_stream
+    lib = binding.load_library()
+
+    def step():
+        st = lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
+                                  wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU, handle)
+        if st != 0:
+            raise binding.TgError(st, "tg_gemm_relu_f16")
+
+    bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    sampler = ClockSampler(bus)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 0)):
+            if flush:
+                scrub.fill_(1.0)
+            step()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        sampler.start()
+        t_all0 = torch.cuda.Event(enable_timing=True)
+        t_all1 = torch.cuda.Event(enable_timing=True)
+        t_all0.record(stream)
+        for i in range(args.steps):
+            if flush:
+                scrub.fill_(1.0)  # L2 flush between timed steps, outside the step's events
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        t_all1.record(stream)
+        stream.synchronize()
+        sampler.stop()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = t_all0.elapsed_time(t_all1)
+    total_ms = sum(step_ms) if flush else region_ms
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps * wl.flops / (total_ms * 1e-3) / 1e12
+    st, word = binding.tg_device_error_check(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} after the timed region")
+
+    # roofline of the dominant kernel (the tcgen05 GEMM); one launch per step when the plan has
+    # a single kernel, so the per-step events bracket exactly that kernel
+    peaks, peak_src = load_peaks()
+    kernel_ms = statistics.mean(step_ms)
+    t_tensor = wl.flops / (peaks["bf16_tflops"] * FP16_OVER_BF16 * 1e12)
+    t_hbm = wl.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = wl.flops / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"] * FP16_OVER_BF16, "unit": "TFLOP/s"}
+    else:
+        achieved = wl.algorithmic_bytes / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic_from_profiles(wl.name) if plan["kernels"] == 1 else None
+    roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json bf16 burst x {FP16_OVER_BF16} "
+                           "fp16/bf16 nominal ratio)" if roof["bound"] == "tensor"
+                           else f"{peak_src} (MEASURED_PEAKS.json copy bandwidth)")
+    roof["kernel_ms"] = kernel_ms
+    roof["t_roof_ms"] = 1e3 * max(t_tensor, t_hbm)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded SplitMix64 inputs of the workload's distribution)",
+        "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+                   "accumulate": "f32", "output": "f16", "epilogue": "relu",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed between steps" if flush else
+                         f"inputs ({in_bytes / 2**20:.0f} MiB) larger than L2",
+                   "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
+                                                 "split_k", "units", "grid", "kernels")}},
+        "gpu_launches": args.steps * plan["kernels"],
+        "roofline": roof,
+        "clocks": sampler.summary(),
+    }
+
+    if rank == 0 and not args.no_e2e:
+        line["e2e"] = e2e(wl, A_h, B_h, dev, max(3, min(args.steps, 10)))
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, a_np, b_np, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e(wl, A_h, B_h, dev, steps):
+    """Same metric through the host-buffer C entry point: H2D of A and B from page-locked
+    memory, the GEMM, D2H of C, all inside the timed region."""
+    import torch
+
+    from fp16_gemm_relu_gb300 import binding
+
+    C_h = torch.empty((wl.M, wl.N), dtype=torch.float16).pin_memory()
+    lib = binding.load_library()
+    stream = torch.cuda.Stream(dev)
+
+    def call():
+        st = lib.tg_gemm_relu_f16_host(A_h.data_ptr(), B_h.data_ptr(), C_h.data_ptr(), wl.M,
+                                       wl.N, wl.K, wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU,
+                                       stream.cuda_stream)
+        if st != 0:
+            raise binding.TgError(st, "tg_gemm_relu_f16_host")
+
+    for _ in range(2):
+        call()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": wl.flops / dt / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": (wl.M * wl.K + wl.K * wl.N) * 2,
+            "d2h_bytes_per_step": wl.M * wl.N * 2, "ms_per_step": 1e3 * dt, "steps": steps}
+
+
+def main():
+    args = parse_args()
+    wl = workloads.get(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

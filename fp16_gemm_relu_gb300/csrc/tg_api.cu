@@ -1,0 +1,603 @@
+// tg_api.cu — the C ABI declared in include/tg_gemm_relu.h.
+//
+// Host side of every call: validate -> plan (tile width, K splits, repack/workspace needs)
+// -> scratch from a stream-ordered pool -> optional operand repack -> TMA tensor maps ->
+// the persistent tcgen05 kernel -> optional deterministic split-K reduction.
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "tg_gemm_relu.h"
+#include "tg_internal.h"
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;  // TMA coordinates are 32-bit
+constexpr int kDefaultPanel = 16;
+constexpr int kDefaultTimeoutMs = 2000;
+constexpr int kBlockNs[3] = {256, 192, 128};
+
+thread_local int t_last_cuda_error = 0;
+
+tg_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return TG_ERR_CUDA;
+}
+
+// Set by kernels whose pipeline wait ran out (see tg_device_error_check).
+__device__ unsigned int g_tg_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  tg_status status = TG_OK;
+  int sm_count = 0;
+  cudaMemPool_t pool = nullptr;
+  unsigned int* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+tg_status current_device(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_devices[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if (major != 10 || minor != 3) {
+      s.status = TG_ERR_UNSUPPORTED_DEVICE;
+    } else {
+      cudaMemPoolProps props;
+      std::memset(&props, 0, sizeof(props));
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      if ((e = cudaMemPoolCreate(&s.pool, &props)) != cudaSuccess) return cuda_fail(e);
+      uint64_t keep = UINT64_MAX;  // keep freed blocks for reuse instead of returning them
+      if ((e = cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+        return cuda_fail(e);
+      if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_tg_error_word)) != cudaSuccess)
+        return cuda_fail(e);
+      s.sm_count = sms;
+      s.status = TG_OK;
+    }
+    s.ready = true;
+  }
+  *out = &s;
+  return s.status;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+tg_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::call_once(g_encode_once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (!g_encode) return cuda_fail(cudaErrorNotSupported);
+  *fn = g_encode;
+  return TG_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+tg_status validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                   int64_t lda, int64_t ldb, int64_t ldc, int flag) {
+  if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TG_ERR_INVALID_ARG;
+  if (flag != TG_EPILOGUE_NONE && flag != TG_EPILOGUE_RELU) return TG_ERR_INVALID_ARG;
+  if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) ||
+      ldc < std::max<int64_t>(1, N))
+    return TG_ERR_INVALID_ARG;
+  if (lda > (int64_t{1} << 36) || ldb > (int64_t{1} << 36) || ldc > (int64_t{1} << 36))
+    return TG_ERR_INVALID_ARG;
+  if (M > 0 && N > 0) {
+    if (C == nullptr) return TG_ERR_INVALID_ARG;
+    if (K > 0 && (A == nullptr || B == nullptr)) return TG_ERR_INVALID_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 1u)
+    return TG_ERR_MISALIGNED;
+  return TG_OK;
+}
+
+struct Plan {
+  tg_plan pub;
+  int64_t lda_p, ldb_p, ldw;     // leading dimensions of the scratch copies / workspace
+  int64_t off_a, off_b, off_w;   // byte offsets inside the scratch block
+};
+
+// Per-k-block cost in SM cycles of an output tile 128 x bn: the tensor-core time (a
+// 128 x bn x 16 MMA takes bn/8 cycles, four per k-block) or the time to bring the stage's
+// bytes in from L2 at ~96 B/cycle, whichever is longer.
+double kblock_cycles(int bn) {
+  const double mma = 2.0 * bn;
+  const double load = (16384.0 + 128.0 * bn) / 96.0;
+  return std::max(mma, load);
+}
+
+// Plan selection (host only): tries every tile width and split count and keeps the fastest
+// by a simple model.  Compute time = waves x k-blocks per unit x kblock_cycles / 1.9 GHz;
+// memory time = the algorithmic bytes at 6.8 TB/s, inflated when a wave keeps fewer than
+// 60% of the SMs busy; plus the float32 workspace traffic of split-K and its extra launch.
+tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N, int64_t K,
+                    int64_t lda, int64_t ldb, int64_t ldc, int num_sms, const tg_options* opt,
+                    Plan* out) {
+  tg_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  if (num_sms <= 0) return TG_ERR_INVALID_ARG;
+  if (o.block_n != 0 && o.block_n != 128 && o.block_n != 192 && o.block_n != 256)
+    return TG_ERR_INVALID_ARG;
+  if (o.split_k < 0 || o.panel_m < 0 || o.max_ctas < 0 || o.timeout_ms < 0)
+    return TG_ERR_INVALID_ARG;
+
+  Plan pl;
+  std::memset(&pl, 0, sizeof(pl));
+  tg_plan& P = pl.pub;
+  P.block_m = tg::kBM;
+  P.block_k = tg::kBK;
+  P.repack_a = (a % 16 != 0 || lda % 8 != 0 || o.force_repack) ? 1 : 0;
+  P.repack_b = (b % 16 != 0 || ldb % 8 != 0 || o.force_repack) ? 1 : 0;
+  const bool c_direct = (c % 16 == 0) && (ldc % 8 == 0) && !o.force_workspace;
+  P.kblocks = cdiv(K, tg::kBK);
+  P.tiles_m = cdiv(M, tg::kBM);
+  if (M == 0 || N == 0) {
+    *out = pl;
+    return TG_OK;
+  }
+  if (K == 0) {  // C = +0: one memset
+    P.kernels = 1;
+    *out = pl;
+    return TG_OK;
+  }
+  const int grid_cap = o.max_ctas > 0 ? std::min(o.max_ctas, num_sms) : num_sms;
+  const double clk = 1.9e9, hbm = 6.8e12;
+  const double alg_bytes = 2.0 * (double(M) * K + double(K) * N + double(M) * N);
+
+  struct Cand {
+    double t;
+    int bn, s, active;
+  };
+  Cand cands[3 * 32];
+  int nc = 0;
+  for (int bn : kBlockNs) {
+    if (o.block_n && bn != o.block_n) continue;
+    const int64_t tiles = P.tiles_m * cdiv(N, bn);
+    const int64_t s_max = o.split_k ? std::min<int64_t>(o.split_k, P.kblocks)
+                                    : std::min<int64_t>(P.kblocks, 32);
+    const int64_t s_min = o.split_k ? s_max : 1;
+    for (int64_t s = s_min; s <= s_max; ++s) {
+      const int64_t kbps = cdiv(P.kblocks, s);
+      const int64_t s_eff = cdiv(P.kblocks, kbps);
+      if (!o.split_k && s_eff != s) continue;  // same plan as a smaller s
+      const int64_t units = tiles * s_eff;
+      const int64_t grid = std::min<int64_t>(units, grid_cap);
+      const int64_t waves = cdiv(units, grid);
+      const bool ws = s_eff > 1 || !c_direct;
+      const double t_mma = double(waves) * double(kbps) * kblock_cycles(bn) / clk;
+      double slots = 0.0;  // wave-by-wave occupancy penalty on the memory time
+      for (int64_t wv = 0; wv < waves; ++wv) {
+        const int64_t active = std::min<int64_t>(grid, units - wv * grid);
+        slots += std::max<double>(double(active), 0.6 * num_sms);
+      }
+      const double t_hbm = alg_bytes / hbm * (slots / double(units));
+      // workspace traffic plus the extra launch of the reduction kernel (~3 us)
+      const double t_ws = ws ? (2.0 * 4.0 * double(s_eff) * M * N + 2.0 * M * N) / hbm + 3e-6 : 0.0;
+      cands[nc++] = Cand{std::max(t_mma, t_hbm) + t_ws, bn, static_cast<int>(s_eff),
+                         static_cast<int>(grid)};
+    }
+  }
+  if (nc == 0) return TG_ERR_INVALID_ARG;
+  double best_t = cands[0].t;
+  for (int i = 1; i < nc; ++i) best_t = std::min(best_t, cands[i].t);
+  // among plans within 2% of the fastest: most SMs busy, then the wider tile, then fewer splits
+  int pick = -1;
+  for (int i = 0; i < nc; ++i) {
+    if (cands[i].t > best_t * 1.02) continue;
+    if (pick < 0 || cands[i].active > cands[pick].active) pick = i;
+  }
+  const int best_bn = cands[pick].bn;
+  const int best_s = cands[pick].s;
+  P.block_n = best_bn;
+  P.stages = tg::gemm_stages(best_bn);
+  P.kblocks_per_split = cdiv(P.kblocks, best_s);
+  P.split_k = static_cast<int>(cdiv(P.kblocks, P.kblocks_per_split));
+  P.tiles_n = cdiv(N, best_bn);
+  P.units = P.tiles_m * P.tiles_n * P.split_k;
+  P.grid = static_cast<int>(std::min<int64_t>(P.units, grid_cap));
+  P.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : kDefaultPanel, P.tiles_m));
+  P.workspace_epilogue = (P.split_k > 1 || !c_direct) ? 1 : 0;
+
+  int64_t off = 0;
+  if (P.repack_a) {
+    pl.lda_p = round_up(K, 8);
+    pl.off_a = off;
+    off += round_up(M * pl.lda_p * 2, 256);
+  }
+  if (P.repack_b) {
+    pl.ldb_p = round_up(N, 8);
+    pl.off_b = off;
+    off += round_up(K * pl.ldb_p * 2, 256);
+  }
+  if (P.workspace_epilogue) {
+    pl.ldw = round_up(N, 4);
+    pl.off_w = off;
+    off += round_up(int64_t(P.split_k) * M * pl.ldw * 4, 256);
+  }
+  P.workspace_bytes = off;
+  P.kernels = 1 + P.repack_a + P.repack_b + P.workspace_epilogue;
+  *out = pl;
+  return TG_OK;
+}
+
+// ------------------------------ auxiliary kernels ------------------------------
+
+// dst (rows x ld_dst, 16-byte aligned rows) <- src (rows x ld_src, any 2-byte alignment).
+// One thread writes 8 consecutive elements with one 16-byte store; columns in
+// [cols, round_up(cols, 8)) are zero.
+__global__ void tg_pack_rows_kernel(const uint16_t* __restrict__ src, int64_t ld_src,
+                                    uint16_t* __restrict__ dst, int64_t ld_dst, int64_t rows,
+                                    int64_t cols) {
+  const int64_t cpr = (cols + 7) >> 3;
+  const int64_t total = rows * cpr;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = idx / cpr;
+    const int64_t c0 = (idx - r * cpr) << 3;
+    const uint16_t* s = src + r * ld_src + c0;
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = (c0 + e < cols) ? __ldg(s + e) : uint16_t(0);
+    uint4 out;
+    out.x = uint32_t(v[0]) | (uint32_t(v[1]) << 16);
+    out.y = uint32_t(v[2]) | (uint32_t(v[3]) << 16);
+    out.z = uint32_t(v[4]) | (uint32_t(v[5]) << 16);
+    out.w = uint32_t(v[6]) | (uint32_t(v[7]) << 16);
+    *reinterpret_cast<uint4*>(dst + r * ld_dst + c0) = out;
+  }
+}
+
+// C[i, j] = fp16(epi(sum_{s=0}^{splits-1} W[s][i][j])), the splits added in increasing s
+// (deterministic).  W rows are ldw floats (multiple of 4, 16-byte aligned); C may have any
+// 2-byte alignment and leading dimension.
+__global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ldw,
+                                        int64_t split_stride, int splits, __half* __restrict__ C,
+                                        int64_t ldc, int64_t M, int64_t N, int relu) {
+  const int64_t cpr = (N + 3) >> 2;
+  const int64_t total = M * cpr;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = idx / cpr;
+    const int64_t c0 = (idx - r * cpr) << 2;
+    const float* w = ws + r * ldw + c0;
+    float4 acc = __ldg(reinterpret_cast<const float4*>(w));
+    for (int s = 1; s < splits; ++s) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(w + s * split_stride));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (relu) {
+      acc.x = acc.x > 0.0f ? acc.x : 0.0f;
+      acc.y = acc.y > 0.0f ? acc.y : 0.0f;
+      acc.z = acc.z > 0.0f ? acc.z : 0.0f;
+      acc.w = acc.w > 0.0f ? acc.w : 0.0f;
+    }
+    __half h[4] = {__float2half_rn(acc.x), __float2half_rn(acc.y), __float2half_rn(acc.z),
+                   __float2half_rn(acc.w)};
+    __half* d = C + r * ldc + c0;
+    if (c0 + 4 <= N && (reinterpret_cast<uintptr_t>(d) & 7u) == 0) {
+      uint2 v;
+      v.x = uint32_t(__half_as_ushort(h[0])) | (uint32_t(__half_as_ushort(h[1])) << 16);
+      v.y = uint32_t(__half_as_ushort(h[2])) | (uint32_t(__half_as_ushort(h[3])) << 16);
+      *reinterpret_cast<uint2*>(d) = v;
+    } else {
+      for (int e = 0; e < 4 && c0 + e < N; ++e) d[e] = h[e];
+    }
+  }
+}
+
+int aux_grid(int64_t work_items, int num_sms) {
+  const int64_t blocks = cdiv(std::max<int64_t>(work_items, 1), 256);
+  return static_cast<int>(std::min<int64_t>(blocks, int64_t(num_sms) * 8));
+}
+
+CUresult encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m,
+                   CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_ws_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, const void* base,
+                      uint64_t n, uint64_t rows, uint64_t splits, uint64_t ldw) {
+  cuuint64_t dims[3] = {n, rows, splits};
+  cuuint64_t strides[2] = {ldw * 4, ldw * 4 * rows};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                   int64_t lda, int64_t ldb, int64_t ldc, int flag, const tg_options* opt,
+                   cudaStream_t stream) {
+  tg_status st = validate(A, B, C, M, N, K, lda, ldb, ldc, flag);
+  if (st != TG_OK) return st;
+  if (M == 0 || N == 0) return TG_OK;
+  DeviceState* ds = nullptr;
+  if ((st = current_device(&ds)) != TG_OK) return st;
+  cudaError_t e;
+  if (K == 0) {
+    e = cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), stream);
+    return e == cudaSuccess ? TG_OK : cuda_fail(e);
+  }
+  Plan pl;
+  st = make_plan(reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
+                 reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, ds->sm_count, opt, &pl);
+  if (st != TG_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if ((st = encode_fn(&enc)) != TG_OK) return st;
+  const tg_plan& P = pl.pub;
+
+  uint8_t* scratch = nullptr;
+  if (P.workspace_bytes > 0) {
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&scratch), size_t(P.workspace_bytes),
+                                ds->pool, stream);
+    if (e != cudaSuccess) {
+      t_last_cuda_error = static_cast<int>(e);
+      return TG_ERR_NO_WORKSPACE;
+    }
+  }
+  auto fail = [&](tg_status s) {
+    if (scratch) cudaFreeAsync(scratch, stream);
+    return s;
+  };
+
+  const void* Ae = A;
+  const void* Be = B;
+  int64_t lda_e = lda, ldb_e = ldb;
+  if (P.repack_a) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pl.off_a);
+    tg_pack_rows_kernel<<<aux_grid(M * cdiv(K, 8), ds->sm_count), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(A), lda, dst, pl.lda_p, M, K);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
+    Ae = dst;
+    lda_e = pl.lda_p;
+  }
+  if (P.repack_b) {
+    uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pl.off_b);
+    tg_pack_rows_kernel<<<aux_grid(K * cdiv(N, 8), ds->sm_count), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(B), ldb, dst, pl.ldb_p, K, N);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
+    Be = dst;
+    ldb_e = pl.ldb_p;
+  }
+
+  tg::GemmLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  CUresult cr = encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(K), uint64_t(M),
+                          uint64_t(lda_e) * 2, tg::kBK, tg::kBM);
+  if (cr == CUDA_SUCCESS)
+    cr = encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(N), uint64_t(K),
+                   uint64_t(ldb_e) * 2, 64, tg::kBK);
+  float* ws = P.workspace_epilogue ? reinterpret_cast<float*>(scratch + pl.off_w) : nullptr;
+  if (cr == CUDA_SUCCESS) {
+    if (ws)
+      cr = encode_ws_3d(enc, &L.out, ws, uint64_t(N), uint64_t(M), uint64_t(P.split_k),
+                        uint64_t(pl.ldw));
+    else
+      cr = encode_2d(enc, &L.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, uint64_t(N), uint64_t(M),
+                     uint64_t(ldc) * 2, 64, 32);
+  }
+  if (cr != CUDA_SUCCESS) return fail(cuda_fail(cudaErrorInvalidValue));
+
+  tg_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  tg::GemmParams& gp = L.p;
+  gp.tiles_m = static_cast<int>(P.tiles_m);
+  gp.tiles_n = static_cast<int>(P.tiles_n);
+  gp.num_kb = static_cast<int>(P.kblocks);
+  gp.kb_per_split = static_cast<int>(P.kblocks_per_split);
+  gp.splits = P.split_k;
+  gp.units = static_cast<int>(P.units);
+  gp.panel_m = P.panel_m;
+  gp.relu = flag == TG_EPILOGUE_RELU ? 1 : 0;
+  gp.debug_flags = o.debug_flags;
+  gp.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : kDefaultTimeoutMs);
+  gp.err = ds->err;
+  L.grid = P.grid;
+  L.stream = stream;
+  switch (P.block_n) {
+    case 256: e = tg::launch_gemm_bn256(L, ws != nullptr); break;
+    case 192: e = tg::launch_gemm_bn192(L, ws != nullptr); break;
+    default: e = tg::launch_gemm_bn128(L, ws != nullptr); break;
+  }
+  if (e != cudaSuccess) return fail(cuda_fail(e));
+
+  if (ws) {
+    tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
+        ws, pl.ldw, int64_t(M) * pl.ldw, P.split_k, static_cast<__half*>(C), ldc, M, N, gp.relu);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
+  }
+  if (scratch && (e = cudaFreeAsync(scratch, stream)) != cudaSuccess) return cuda_fail(e);
+  return TG_OK;
+}
+
+}  // namespace
+
+namespace tg {
+int gemm_stages(int block_n) {
+  switch (block_n) {
+    case 256: return TileCfg<256>::kStages;
+    case 192: return TileCfg<192>::kStages;
+    default: return TileCfg<128>::kStages;
+  }
+}
+int gemm_smem_bytes(int block_n) {
+  switch (block_n) {
+    case 256: return TileCfg<256>::kSmemBytes;
+    case 192: return TileCfg<192>::kSmemBytes;
+    default: return TileCfg<128>::kSmemBytes;
+  }
+}
+}  // namespace tg
+
+// ------------------------------ exported C ABI ------------------------------
+extern "C" {
+
+tg_status tg_gemm_relu_f16(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                           int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue_flag,
+                           tg_stream_t stream) {
+  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc, epilogue_flag, nullptr,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tg_gemm_relu_f16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              int epilogue_flag, const tg_options* opt, tg_stream_t stream) {
+  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc, epilogue_flag, opt,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tg_plan_query(const void* A, const void* B, const void* C, int64_t M, int64_t N,
+                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int num_sms,
+                        const tg_options* opt, tg_plan* out) {
+  if (out == nullptr) return TG_ERR_INVALID_ARG;
+  tg_status st = validate(A, B, C, M, N, K, lda, ldb, ldc, TG_EPILOGUE_RELU);
+  if (st != TG_OK) return st;
+  Plan pl;
+  st = make_plan(reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
+                 reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, num_sms, opt, &pl);
+  if (st == TG_OK) *out = pl.pub;
+  return st;
+}
+
+tg_status tg_gemm_relu_f16_host(const void* hA, const void* hB, void* hC, int64_t M, int64_t N,
+                                int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                int epilogue_flag, tg_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  tg_status st = validate(hA, hB, hC, M, N, K, lda, ldb, ldc, epilogue_flag);
+  if (st != TG_OK) return st;
+  if (M == 0 || N == 0) return TG_OK;
+  DeviceState* ds = nullptr;
+  if ((st = current_device(&ds)) != TG_OK) return st;
+  // device copies with 16-byte aligned rows, so the direct (TMA) path applies
+  const int64_t lda_d = round_up(std::max<int64_t>(K, 1), 8);
+  const int64_t ldb_d = round_up(N, 8);
+  const int64_t ldc_d = round_up(N, 8);
+  const int64_t bytes_a = round_up(M * lda_d * 2, 256);
+  const int64_t bytes_b = round_up(std::max<int64_t>(K, 1) * ldb_d * 2, 256);
+  const int64_t bytes_c = round_up(M * ldc_d * 2, 256);
+  uint8_t* buf = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf),
+                                          size_t(bytes_a + bytes_b + bytes_c), ds->pool, stream);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = static_cast<int>(e);
+    return TG_ERR_NO_WORKSPACE;
+  }
+  uint8_t* dA = buf;
+  uint8_t* dB = buf + bytes_a;
+  uint8_t* dC = buf + bytes_a + bytes_b;
+  st = TG_OK;
+  if (K > 0) {
+    if ((e = cudaMemcpy2DAsync(dA, size_t(lda_d) * 2, hA, size_t(lda) * 2, size_t(K) * 2,
+                               size_t(M), cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaMemcpy2DAsync(dB, size_t(ldb_d) * 2, hB, size_t(ldb) * 2, size_t(N) * 2,
+                               size_t(K), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+      st = cuda_fail(e);
+  }
+  if (st == TG_OK)
+    st = run_gemm(dA, dB, dC, M, N, K, lda_d, ldb_d, ldc_d, epilogue_flag, nullptr, stream);
+  if (st == TG_OK &&
+      (e = cudaMemcpy2DAsync(hC, size_t(ldc) * 2, dC, size_t(ldc_d) * 2, size_t(N) * 2,
+                             size_t(M), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+    st = cuda_fail(e);
+  cudaFreeAsync(buf, stream);
+  if ((e = cudaStreamSynchronize(stream)) != cudaSuccess && st == TG_OK) st = cuda_fail(e);
+  if (st == TG_OK) {
+    unsigned int word = 0;
+    if ((e = cudaMemcpyFromSymbol(&word, g_tg_error_word, sizeof(word))) != cudaSuccess)
+      st = cuda_fail(e);
+    else if (word != 0)
+      st = TG_ERR_TIMEOUT;
+  }
+  return st;
+}
+
+tg_status tg_device_error_check(unsigned* out_word, int clear) {
+  DeviceState* ds = nullptr;
+  tg_status st = current_device(&ds);
+  if (st != TG_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int word = 0;
+  if ((e = cudaMemcpyFromSymbol(&word, g_tg_error_word, sizeof(word))) != cudaSuccess)
+    return cuda_fail(e);
+  if (clear) {
+    const unsigned int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_tg_error_word, &zero, sizeof(zero))) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if (out_word) *out_word = word;
+  return word ? TG_ERR_TIMEOUT : TG_OK;
+}
+
+const char* tg_status_string(tg_status s) {
+  switch (s) {
+    case TG_OK: return "ok";
+    case TG_ERR_INVALID_ARG: return "invalid argument";
+    case TG_ERR_MISALIGNED: return "pointer not 2-byte aligned";
+    case TG_ERR_UNSUPPORTED_DEVICE: return "unsupported device (compute capability 10.3 required)";
+    case TG_ERR_CUDA: return "CUDA error (see tg_last_cuda_error)";
+    case TG_ERR_TIMEOUT: return "kernel pipeline wait timed out";
+    case TG_ERR_NO_WORKSPACE: return "scratch memory unavailable";
+  }
+  return "unknown status";
+}
+
+tg_status tg_last_cuda_error(int* cuda_err) {
+  if (cuda_err == nullptr) return TG_ERR_INVALID_ARG;
+  *cuda_err = t_last_cuda_error;
+  return TG_OK;
+}
+
+tg_status tg_release_workspace(void) {
+  DeviceState* ds = nullptr;
+  tg_status st = current_device(&ds);
+  if (st != TG_OK) return st;
+  cudaError_t e = cudaMemPoolTrimTo(ds->pool, 0);
+  return e == cudaSuccess ? TG_OK : cuda_fail(e);
+}
+
+int tg_version(void) { return 100; }
+
+}  // extern "C"

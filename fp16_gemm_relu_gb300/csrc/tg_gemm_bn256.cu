@@ -1,0 +1,24 @@
+// Instantiation of the tcgen05 kernel for 256-wide output tiles (its own translation unit
+// so that the tile widths compile in parallel).
+#include "tg_internal.h"
+
+namespace tg {
+
+namespace {
+template <bool OUT_F32>
+cudaError_t launch_one(const GemmLaunch& l) {
+  auto kern = tg_gemm_tc_kernel<256, OUT_F32>;
+  constexpr int smem = TileCfg<256>::kSmemBytes;
+  // per device and per function; cheap enough to repeat on every launch
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<l.grid, kThreads, smem, l.stream>>>(l.a, l.b, l.out, l.p);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemm_bn256(const GemmLaunch& l, bool out_f32) {
+  return out_f32 ? launch_one<true>(l) : launch_one<false>(l);
+}
+
+}  // namespace tg

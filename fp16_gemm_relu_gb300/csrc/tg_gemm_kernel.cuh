@@ -1,0 +1,579 @@
+// tg_gemm_kernel.cuh — persistent, warp-specialised tcgen05 kernel for C = epi(A·B), sm_103a.
+//
+// The method is the matmul_relu tile program of the TileLang paper-reading page (section 2):
+// per output tile, clear a float32 accumulator, loop over K in pipelined stages that copy an
+// A tile and a B tile into shared memory and accumulate their product, then apply max(x, 0)
+// elementwise and copy the tile out as fp16.  Section 4 of the same page adds the L2-friendly
+// tile order (T.use_swizzle).  The pages' design targets register-file accumulators on
+// sm_80/sm_90; this one is written for Blackwell:
+//
+//   warp 0   producer: one thread issues TMA loads (128B-swizzled boxes) into an S-stage
+//            shared-memory ring; full[s]/empty[s] mbarriers hand stages to the MMA thread.
+//   warp 1   MMA issuer: allocates tensor memory (TMEM), one thread issues
+//            tcgen05.mma.cta_group::1.kind::f16 (128 x BN x 16 per instruction, fp16 in,
+//            fp32 accumulate) and tcgen05.commit to release stages; two TMEM accumulators
+//            let the epilogue of tile t overlap the main loop of tile t+1.
+//   warps 2-5 epilogue: tcgen05.ld the accumulator (each warp owns a 32-lane quarter of
+//            TMEM = 32 rows), apply relu (or nothing), round to fp16 (or keep fp32 for a
+//            split-K partial), stage the rows in 128B-swizzled shared memory and write them
+//            with TMA stores, which clip the M/N tails.
+//
+// The grid is persistent: CTA b processes work units b, b + gridDim.x, ...  A unit is one
+// (split, tile) pair; tiles are ordered in panels of panel_m M-tiles so that CTAs running at
+// the same time share A and B panels in L2.
+//
+// Every mbarrier wait is bounded (p.timeout_ns, measured on %globaltimer); when one runs out
+// the thread records the role in *p.err, raises a CTA-wide abort flag and every role drains
+// what it has in flight (TMA loads, MMAs, TMA stores) before TMEM is freed and the CTA exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace tg {
+
+constexpr int kBM = 128;          // UMMA M (TMEM lanes)
+constexpr int kBK = 64;           // K per stage: 64 fp16 = 128 bytes = one 128B swizzle row
+constexpr int kUmmaK = 16;        // K per tcgen05.mma.kind::f16
+constexpr int kThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr int kStagingBuf = 32 * 128;  // one epilogue warp's 32 rows x 128 bytes
+constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory per block
+constexpr int kSmemReserve = 1024 + 256;
+
+enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+enum : int { kDebugDropFirstStage = 1 };
+
+struct GemmParams {
+  int tiles_m, tiles_n;
+  int num_kb;          // ceil(K / kBK)
+  int kb_per_split;
+  int splits;
+  int units;           // tiles_m * tiles_n * splits
+  int panel_m;
+  int relu;
+  int debug_flags;
+  unsigned long long timeout_ns;
+  unsigned int* err;
+};
+
+template <int BN>
+struct TileCfg {
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN must be 64..256 in steps of 64");
+  static constexpr int kAStage = kBM * kBK * 2;                 // 16 KB
+  static constexpr int kBBox = kBK * 64 * 2;                    // one 64(N) x 64(K) box, 8 KB
+  static constexpr int kBStage = kBK * BN * 2;
+  static constexpr int kStageBytes = kAStage + kBStage;
+  static constexpr int kStagingBytes = kEpiWarps * 2 * kStagingBuf;
+  static constexpr int kStagesFit = (kSmemLimit - kSmemReserve - kStagingBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kAccStride = BN <= 128 ? 128 : 256;      // TMEM columns per accumulator
+  static constexpr int kTmemCols = 2 * kAccStride;              // power of two >= 32
+  static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes + kStagingBytes;
+  static_assert(kStages >= 2, "not enough shared memory for a pipeline");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
+};
+
+// ---------------------------------------------------------------------------------------
+// PTX wrappers (PTX ISA: mbarrier, cp.async.bulk.tensor, tcgen05)
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   holder_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]; accumulate == 0 overwrites D (the cleared
+// accumulator of the tile program).
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns: thread l of the warp gets lane (base + l).
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+// Wait for this thread's outstanding tcgen05.ld; the registers are threaded through the asm
+// so that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------------------
+// Descriptors (PTX ISA, tcgen05 "matrix descriptor" and "instruction descriptor")
+// ---------------------------------------------------------------------------------------
+// Shared-memory matrix descriptor, 128-byte swizzle:
+//   [0,14) start address >> 4, [16,30) leading byte offset >> 4, [32,46) stride byte
+//   offset >> 4, [46,49) fixed 0b001, [49,52) base offset (0: atoms are 1024-byte aligned),
+//   [52] LBO mode (0), [61,64) layout: 2 = SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 2ull << 61;
+  return d;
+}
+
+// A tile: 128 rows (M) x 64 K, K contiguous ("K-major"); row r at r*128 bytes, 16-byte chunks
+// XOR-swizzled by r%8.  Canonical K-major SW128: 8-row groups 1024 bytes apart (SBO); LBO is
+// unused for swizzled K-major layouts (encoded as 16 bytes).  The k-th 16-wide K slice
+// starts 32*k bytes into the rows.
+__device__ __forceinline__ uint64_t desc_a_kmajor(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
+
+// B tile: 64 K rows x BN, N contiguous ("MN-major"), stored as BN/64 boxes of 64(N) x 64(K),
+// each box 8 KB with K row r at r*128 bytes.  Canonical MN-major SW128: consecutive 64-wide
+// N chunks are LBO = 8 KB apart, consecutive groups of 8 K rows are SBO = 1024 bytes apart.
+// The k-th 16-deep K slice starts 16*128*k = 2048*k bytes in.
+__device__ __forceinline__ uint64_t desc_b_mnmajor(uint32_t saddr) { return sw128_desc(saddr, 8192, 1024); }
+
+// Instruction descriptor for kind::f16: D f32 (bits 4-5 = 1), A f16 (7-9 = 0), B f16
+// (10-12 = 0), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N>>3 at 17-22, M>>4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------------------
+// Work decomposition
+// ---------------------------------------------------------------------------------------
+struct Unit {
+  int m_blk, n_blk, split, kb_begin, kb_end;
+};
+
+// Unit u -> (split, tile); splits are the outer index so that co-running CTAs share a K range.
+// Tiles walk panels of panel_m M-tiles, M-tile fastest inside a panel (T.use_swizzle-style
+// rasterisation, TileLang paper-reading page, section 4).
+__device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
+  Unit w;
+  const int tiles = p.tiles_m * p.tiles_n;
+  w.split = u / tiles;
+  const int t = u - w.split * tiles;
+  const int group = p.panel_m * p.tiles_n;
+  const int g = t / group;
+  const int r = t - g * group;
+  const int first_m = g * p.panel_m;
+  const int rows = min(p.panel_m, p.tiles_m - first_m);
+  w.m_blk = first_m + r % rows;
+  w.n_blk = r / rows;
+  w.kb_begin = w.split * p.kb_per_split;
+  w.kb_end = min(w.kb_begin + p.kb_per_split, p.num_kb);
+  return w;
+}
+
+// Bounded wait.  Returns false when the CTA is aborting or this wait ran out (then it raises
+// the abort flag and records the role in *p.err).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
+                                           volatile uint32_t* abort_flag, const GemmParams& p,
+                                           uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        *abort_flag = 1u;
+        __threadfence_block();
+        atomicOr(p.err, 1u | (role << 8));
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait that ignores the abort flag: used while draining work already in flight.
+__device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity,
+                                                 const GemmParams& p) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > p.timeout_ns) return false;
+  }
+}
+
+__device__ __forceinline__ uint32_t relu_pack_h2(uint32_t a, uint32_t b, int relu) {
+  float x = __uint_as_float(a);
+  float y = __uint_as_float(b);
+  if (relu) {
+    x = (x > 0.0f) ? x : 0.0f;  // -0 and NaN become +0
+    y = (y > 0.0f) ? y : 0.0f;
+  }
+  __half2 h = __floats2half2_rn(x, y);  // round to nearest even; x in the low half
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------------------
+// tmA:   fp16 A, dims {K, M}, box {64, 128}, 128B swizzle
+// tmB:   fp16 B, dims {N, K}, box {64, 64}, 128B swizzle
+// tmOut: OUT_F32 == false: fp16 C, dims {N, M}, box {64, 32}, 128B swizzle
+//        OUT_F32 == true:  f32 workspace, dims {N, M, splits}, box {32, 32, 1}, 128B swizzle
+template <int BN, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+    tg_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  using Cfg = TileCfg<BN>;
+  constexpr int S = Cfg::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * Cfg::kAStage;
+  uint8_t* sStg = sB + S * Cfg::kBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStagingBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool dropped = false;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
+            goto producer_done;
+          if ((p.debug_flags & kDebugDropFirstStage) && blockIdx.x == 0 && !dropped) {
+            dropped = true;  // injected fault: this stage is never filled
+          } else {
+            const uint32_t fb = smem_u32(&full[stage]);
+            mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+            tma_load_2d(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, w.m_blk * kBM);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_2d(smem_u32(sB + stage * Cfg::kBStage + j * Cfg::kBBox), &tmB, fb,
+                          w.n_blk * BN + j * 64, kb * kBK);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    producer_done:
+      // no TMA load may still be writing shared memory when the CTA exits
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) wait_phase_drain(smem_u32(&full[s]), (armed_parity >> s) & 1u, p);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+        const Unit w = unit_of(p, u);
+        const int buf = t & 1;
+        const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+        if (!wait_phase(smem_u32(&tempty[buf]), use ^ 1u, abort_flag, p, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        bool ok = true;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&full[stage]), phase, abort_flag, p, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_a_kmajor(smem_u32(sA + stage * Cfg::kAStage));
+          const uint64_t bd = desc_b_mnmajor(smem_u32(sB + stage * Cfg::kBStage));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            // start-address field is in 16-byte units: A advances 32 B, B advances 2048 B
+            umma_f16(d_tmem, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(128 * k),
+                     idesc, (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&empty[stage]));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[buf]));
+      }
+      // every MMA issued by this thread has finished before TMEM can be released
+      umma_commit(smem_u32(drain));
+      wait_phase_drain(smem_u32(drain), 0u, p);
+    }
+  } else {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int ew = warp - 2;      // staging slot
+    uint8_t* stg = sStg + ew * 2 * kStagingBuf;
+    int sb = 0;
+    int t = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+      const Unit w = unit_of(p, u);
+      const int buf = t & 1;
+      const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const int row0 = w.m_blk * kBM + q * 32;
+      if constexpr (!OUT_F32) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_x32(tl + c * 64, r0);
+          tmem_wait_ld(r0);
+          tmem_ld_x32(tl + c * 64 + 32, r1);
+          tmem_wait_ld(r1);
+          if (c == BN / 64 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.relu);
+            pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.relu);
+          }
+          uint8_t* st = stg + sb * kStagingBuf;
+          if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmOut, smem_u32(st), w.n_blk * BN + c * 64, row0);
+            bulk_commit();
+          }
+          sb ^= 1;
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld_x32(tl + c * 32, r);
+          tmem_wait_ld(r);
+          if (c == BN / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+          }
+          uint8_t* st = stg + sb * kStagingBuf;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4 v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmOut, smem_u32(st), w.n_blk * BN + c * 32, row0, w.split);
+            bulk_commit();
+          }
+          sb ^= 1;
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace tg

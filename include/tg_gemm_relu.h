@@ -1,0 +1,148 @@
+/*
+ * tg_gemm_relu.h — C ABI of the GB300 (sm_103a) relu(A·B) library.
+ *
+ * The operation (TileLang paper-reading page, section 2, the matmul_relu example; the
+ * practitioner page, section 3.2, on the float32 accumulator):
+ *
+ *     C[i,j] = fp16( epilogue( sum_{k<K} A[i,k] * B[k,j] ) )    0 <= i < M, 0 <= j < N
+ *
+ * A is M x K and B is K x N, both row-major IEEE binary16 ("fp16"); the sum is accumulated in
+ * binary32 on the tensor cores; epilogue is relu(x) = (x > 0 ? x : +0) or the identity; the
+ * result is rounded to fp16 with round-to-nearest-even and written to the row-major M x N C.
+ * The summation order inside the sum is the kernel's blocked order (not specified); for a
+ * given plan it is fixed, so results are bitwise reproducible run to run, split-K included.
+ *
+ * Conventions shared by every entry point:
+ *  - Leading dimensions are in elements: element (i,k) of A is A[i*lda + k], and so on.
+ *    lda >= max(1,K), ldb >= max(1,N), ldc >= max(1,N).
+ *  - Pointers must be 2-byte aligned (TG_ERR_MISALIGNED otherwise). 16-byte aligned pointers
+ *    with leading dimensions that are multiples of 8 take the direct path; anything else is
+ *    handled too (operands are first repacked into aligned scratch, C goes through a float32
+ *    scratch and a final conversion pass).
+ *  - M == 0 or N == 0 is a no-op. K == 0 writes +0 to every element of C.
+ *  - C must not overlap A or B (not checked).
+ *  - Errors are detected on the host before anything is launched; a call that returns an
+ *    error has launched nothing and written nothing.
+ *  - Device support: compute capability 10.3 (GB300) only (TG_ERR_UNSUPPORTED_DEVICE).
+ *  - Thread safety: every entry point may be called from several host threads at once.
+ */
+#ifndef TG_GEMM_RELU_H
+#define TG_GEMM_RELU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* tg_stream_t;
+
+typedef enum {
+  TG_OK = 0,
+  TG_ERR_INVALID_ARG = 1,        /* negative size, short leading dimension, NULL, bad flag */
+  TG_ERR_MISALIGNED = 2,         /* a pointer that is not 2-byte aligned */
+  TG_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+  TG_ERR_CUDA = 4,               /* a CUDA call failed; see tg_last_cuda_error */
+  TG_ERR_TIMEOUT = 5,            /* a kernel gave up waiting on a pipeline barrier */
+  TG_ERR_NO_WORKSPACE = 6        /* scratch memory could not be obtained */
+} tg_status;
+
+enum { TG_EPILOGUE_NONE = 0, TG_EPILOGUE_RELU = 1 };
+
+/*
+ * C = fp16(relu(A·B)) (epilogue_flag = TG_EPILOGUE_RELU) or C = fp16(A·B) (TG_EPILOGUE_NONE).
+ * A, B, C: device pointers to fp16 data, owned by the caller.  Asynchronous on `stream`:
+ * returns once the work is queued; the caller synchronises.  Scratch memory, when a plan
+ * needs it, comes from a library-owned stream-ordered pool on the current device and is
+ * released back to the pool in stream order (see tg_release_workspace).
+ */
+tg_status tg_gemm_relu_f16(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                           int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue_flag,
+                           tg_stream_t stream);
+
+/* Plan overrides, for tests and tuning.  Zero-initialise; every zero field means "choose". */
+typedef struct {
+  int block_n;          /* 0, or the N extent of an output tile: 128, 192 or 256 */
+  int split_k;          /* 0, or the number of K splits (>= 1) */
+  int force_repack;     /* 1: copy A and B into aligned scratch even when not needed */
+  int force_workspace;  /* 1: write C through the float32 scratch and conversion pass */
+  int panel_m;          /* 0, or the L2 panel height in M tiles for the tile order */
+  int max_ctas;         /* 0 (one per SM), or a cap on the persistent grid */
+  int debug_flags;      /* TG_DEBUG_* below; 0 in normal use */
+  int timeout_ms;       /* 0 (default 2000 ms), or the per-wait limit of the pipeline */
+} tg_options;
+
+/* Fault injection: the first producer of the grid drops its first stage (no load, no
+ * arrival), so the consumer's wait on that stage runs out; the kernel records the timeout,
+ * drains and returns.  Only for the error-path test. */
+#define TG_DEBUG_DROP_FIRST_STAGE 1
+
+/* What a call will do; filled by tg_plan_query (host only, no device needed). */
+typedef struct {
+  int block_m, block_n, block_k, stages;
+  int split_k;                 /* K splits actually used */
+  int64_t kblocks;             /* ceil(K / block_k) */
+  int64_t kblocks_per_split;
+  int64_t tiles_m, tiles_n;
+  int64_t units;               /* tiles_m * tiles_n * split_k work units */
+  int grid;                    /* persistent CTAs */
+  int panel_m;
+  int repack_a, repack_b;      /* operand copied into aligned scratch first */
+  int workspace_epilogue;      /* C produced by the float32 scratch + conversion pass */
+  int64_t workspace_bytes;     /* scratch needed per call */
+  int kernels;                 /* kernel launches per call */
+} tg_plan;
+
+/*
+ * Same as tg_gemm_relu_f16 with plan overrides (opt may be NULL).  An override that the
+ * shape cannot honour (for example split_k larger than the number of K blocks) is clamped.
+ */
+tg_status tg_gemm_relu_f16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                              int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                              int epilogue_flag, const tg_options* opt, tg_stream_t stream);
+
+/*
+ * The plan tg_gemm_relu_f16_ex would use for these arguments on a device with num_sms SMs.
+ * The pointers are used only for their alignment.  Pure host function.
+ */
+tg_status tg_plan_query(const void* A, const void* B, const void* C, int64_t M, int64_t N,
+                        int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int num_sms,
+                        const tg_options* opt, tg_plan* out);
+
+/*
+ * End-to-end call on HOST buffers: copies A and B (host, row-major with lda/ldb) to the
+ * current device, runs the GEMM on `stream`, copies C back into the host buffer (ldc) and
+ * synchronises `stream` before returning.  Page-locked host memory gives the fastest copies.
+ * Device buffers come from the library pool.  Also reports a kernel timeout
+ * (TG_ERR_TIMEOUT), which the asynchronous entry points cannot.
+ */
+tg_status tg_gemm_relu_f16_host(const void* hA, const void* hB, void* hC, int64_t M,
+                                int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                int epilogue_flag, tg_stream_t stream);
+
+/*
+ * Reads the current device's error word that the kernels set when a pipeline wait runs out
+ * (bit 0: timeout; bits 8..15: the role that gave up: 1 producer, 2 MMA, 3 epilogue).
+ * Synchronises the device.  clear != 0 resets the word.  Returns TG_ERR_TIMEOUT if set.
+ */
+tg_status tg_device_error_check(unsigned* out_word, int clear);
+
+/* Static text for a status code (never NULL). */
+const char* tg_status_string(tg_status status);
+
+/* The cudaError_t value behind the calling thread's last TG_ERR_CUDA (0 if none). */
+tg_status tg_last_cuda_error(int* cuda_err);
+
+/* Returns the library pool's unused scratch memory on the current device to the system. */
+tg_status tg_release_workspace(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int tg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TG_GEMM_RELU_H */

@@ -1,0 +1,122 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and its host-only
+logic (argument validation, plan selection, status strings) behaves as documented."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp16_gemm_relu_gb300 as tg
+from fp16_gemm_relu_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp16_gemm_relu_gb300 import build
+
+    build.build()
+    return tg.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(tg_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "tg_gemm_relu_f16" in names and len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert binding.tg_status_string(s)
+    assert binding.tg_status_string(99) == "unknown status"
+    assert binding.tg_version() == 100
+
+
+def test_validation_before_any_device_work(lib):
+    # these return from host validation, before any CUDA call
+    p = 4096
+    assert binding.tg_gemm_relu_f16(p, p, p, -1, 4, 4, 4, 4, 4, 1) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(p, p, p, 4, 4, 4, 3, 4, 4, 1) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(p, p, p, 4, 4, 4, 4, 3, 4, 1) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(p, p, p, 4, 4, 4, 4, 4, 3, 1) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(p, p, p, 4, 4, 4, 4, 4, 4, 2) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(0, p, p, 4, 4, 4, 4, 4, 4, 1) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(p, p, 0, 4, 4, 4, 4, 4, 4, 1) == binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16(p + 1, p, p, 4, 4, 4, 4, 4, 4, 1) == binding.TG_ERR_MISALIGNED
+    assert binding.tg_gemm_relu_f16(p, p, p + 1, 4, 4, 4, 4, 4, 4, 1) == binding.TG_ERR_MISALIGNED
+    # empty output: a no-op that succeeds
+    assert binding.tg_gemm_relu_f16(0, 0, 0, 0, 5, 5, 5, 5, 5, 1) == binding.TG_OK
+    assert binding.tg_gemm_relu_f16(0, 0, 0, 5, 0, 5, 5, 1, 1, 1) == binding.TG_OK
+    assert binding.tg_gemm_relu_f16_host(0, 0, 0, -3, 1, 1, 1, 1, 1, 1) == binding.TG_ERR_INVALID_ARG
+    st, _ = binding.tg_plan_query(p, p, p, 4, 4, 4, 4, 4, 4, 0)
+    assert st == binding.TG_ERR_INVALID_ARG
+    st, _ = binding.tg_plan_query(p, p, p, 4, 4, 4, 4, 4, 4, 152, {"block_n": 96})
+    assert st == binding.TG_ERR_INVALID_ARG
+
+
+def _plan(M, N, K, **kw):
+    opts = kw.pop("options", None)
+    return tg.plan(M, N, K, options=opts, **kw)
+
+
+def test_plan_square_is_one_kernel_wide_tiles(lib):
+    p = _plan(8192, 8192, 8192)
+    assert (p["block_m"], p["block_n"], p["block_k"]) == (128, 256, 64)
+    assert p["split_k"] == 1 and p["kernels"] == 1 and p["workspace_bytes"] == 0
+    assert p["tiles_m"] == 64 and p["tiles_n"] == 32 and p["units"] == 2048
+    assert p["grid"] == 152 and p["stages"] == 4
+
+
+def test_plan_skinny_fills_the_machine(lib):
+    p = _plan(64, 28672, 8192)
+    assert p["units"] >= 0.95 * 152 or p["split_k"] > 1
+    assert p["grid"] >= 140
+
+
+def test_plan_ragged_unaligned(lib):
+    # odd leading dimensions: operands are repacked, C goes through the fp32 workspace
+    p = _plan(4095, 3073, 65537)
+    assert p["repack_a"] == 1 and p["repack_b"] == 1 and p["workspace_epilogue"] == 1
+    assert p["kernels"] == 4
+    assert p["kblocks"] == 1025
+    assert p["split_k"] * p["kblocks_per_split"] >= 1025
+    assert (p["split_k"] - 1) * p["kblocks_per_split"] < 1025
+    ws = 4095 * 65544 * 2 + 65537 * 3080 * 2 + p["split_k"] * 4095 * 3076 * 4
+    assert p["workspace_bytes"] >= ws
+
+
+def test_plan_alignment_from_pointers(lib):
+    a = _plan(256, 256, 256, a_ptr=258)
+    assert a["repack_a"] == 1 and a["repack_b"] == 0 and a["workspace_epilogue"] == 0
+    c = _plan(256, 256, 256, c_ptr=264)
+    assert c["workspace_epilogue"] == 1
+
+
+def test_plan_overrides(lib):
+    p = _plan(1000, 1000, 1000, options={"block_n": 128, "split_k": 3, "max_ctas": 5,
+                                          "panel_m": 2})
+    assert p["block_n"] == 128 and p["split_k"] == 3 and p["grid"] == 5 and p["panel_m"] == 2
+    assert p["workspace_epilogue"] == 1 and p["units"] == 8 * 8 * 3
+    # more splits than K blocks are clamped, and no split is empty
+    q = _plan(100, 100, 130, options={"split_k": 50})
+    assert q["split_k"] == 3 and q["kblocks_per_split"] == 1
+    r = _plan(100, 100, 1000, options={"split_k": 6})
+    assert (r["split_k"] - 1) * r["kblocks_per_split"] < r["kblocks"]
+
+
+def test_plan_k_zero_and_empty(lib):
+    assert _plan(10, 10, 0)["kernels"] == 1
+    assert _plan(0, 10, 10)["kernels"] == 0

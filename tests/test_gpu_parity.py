@@ -1,0 +1,232 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, element by element, on seeded
+inputs: every tile width, split-K on and off, repacked operands, the workspace epilogue,
+multi-tile-per-CTA schedules, ragged tails, odd leading dimensions and pointers, empty and
+degenerate shapes, and the integer-input case where any summation order is exact."""
+
+import numpy as np
+import pytest
+
+import oracle
+from fp16_gemm_relu_gb300 import binding, inputs
+
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from fp16_gemm_relu_gb300 import build
+
+    build.build()
+    binding.load_library()
+    torch.cuda.set_device(0)
+    yield
+    st, word = binding.tg_device_error_check(clear=True)
+    assert st == binding.TG_OK, f"device error word {word:#x}"
+
+
+def _dev(x: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def run_gpu(a, b, relu=True, options=None, lda=None, ldb=None, ldc=None, a_off=0, b_off=0,
+            c_off=0, fill=np.nan):
+    """Run through tg_gemm_relu_f16(_ex) with optional padded leading dimensions and element
+    offsets of the base pointers (odd offsets give 2-byte-aligned pointers).  Returns the C
+    bits (M, N) and the untouched-canary check of the padding."""
+    M, K = a.shape
+    N = b.shape[1]
+    lda = lda or max(K, 1)
+    ldb = ldb or max(N, 1)
+    ldc = ldc or max(N, 1)
+    abuf = np.full(a_off + M * lda + 8, fill, dtype=np.float16)
+    abuf[a_off:a_off + M * lda].reshape(M, lda)[:, :K] = a
+    bbuf = np.full(b_off + K * ldb + 8, fill, dtype=np.float16)
+    bbuf[b_off:b_off + K * ldb].reshape(K, ldb)[:, :N] = b
+    canary = np.uint16(0x7E5A)
+    cbuf = np.full(c_off + M * ldc + 8, canary, dtype=np.uint16)
+    dA, dB, dC = _dev(abuf), _dev(bbuf), _dev(cbuf)
+    pa = dA.data_ptr() + 2 * a_off
+    pb = dB.data_ptr() + 2 * b_off
+    pc = dC.data_ptr() + 2 * c_off
+    flag = binding.TG_EPILOGUE_RELU if relu else binding.TG_EPILOGUE_NONE
+    stream = torch.cuda.current_stream().cuda_stream
+    if options is None:
+        st = binding.tg_gemm_relu_f16(pa, pb, pc, M, N, K, lda, ldb, ldc, flag, stream)
+    else:
+        st = binding.tg_gemm_relu_f16_ex(pa, pb, pc, M, N, K, lda, ldb, ldc, flag, options, stream)
+    assert st == binding.TG_OK, binding.tg_status_string(st)
+    torch.cuda.synchronize()
+    out = dC.cpu().numpy()
+    c = out[c_off:c_off + M * ldc].reshape(M, ldc)
+    pad_ok = bool((c[:, N:] == canary).all() and (out[:c_off] == canary).all()
+                  and (out[c_off + M * ldc:] == canary).all())
+    return np.ascontiguousarray(c[:, :N]), pad_ok
+
+
+def oracle_ref(a, b, relu=True, rows=None, cols=None):
+    return oracle.gemm_relu(a, b, relu=relu, rows=rows, cols=cols)
+
+
+SHAPES = [(1, 1, 1), (7, 13, 5), (128, 256, 64), (129, 257, 65), (255, 300, 1000),
+          (300, 520, 777), (64, 1000, 3000), (1000, 777, 1031)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("relu", [True, False])
+def test_default_plan_parity(M, N, K, relu):
+    a = inputs.tensor(M, K, 1000 + M, 0)
+    b = inputs.tensor(K, N, 1000 + M, 1)
+    c, pad_ok = run_gpu(a, b, relu)
+    assert pad_ok
+    assert_parity(c, oracle_ref(a, b, relu), K, relu, where=f"{M}x{N}x{K}")
+
+
+FORCED = [
+    {"block_n": 256}, {"block_n": 192}, {"block_n": 128},
+    {"split_k": 2}, {"split_k": 3, "block_n": 192}, {"split_k": 7, "block_n": 128},
+    {"force_repack": 1}, {"force_workspace": 1},
+    {"max_ctas": 1}, {"max_ctas": 3, "split_k": 2}, {"max_ctas": 5, "panel_m": 1},
+    {"max_ctas": 2, "block_n": 128, "panel_m": 2},
+]
+
+
+@pytest.mark.parametrize("opts", FORCED, ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
+def test_forced_plans_parity(opts):
+    M, N, K = 300, 600, 1500
+    a = inputs.tensor(M, K, 77, 0)
+    b = inputs.tensor(K, N, 77, 1)
+    c, pad_ok = run_gpu(a, b, True, options=opts)
+    assert pad_ok
+    assert_parity(c, oracle_ref(a, b, True), K, True, where=str(opts))
+
+
+@pytest.mark.parametrize("opts", [None, {"split_k": 4}, {"max_ctas": 3}, {"force_repack": 1,
+                                                                            "split_k": 3}])
+@pytest.mark.parametrize("M,N,K", [(200, 300, 700), (129, 65, 4099)])
+def test_integer_inputs_bitwise(opts, M, N, K):
+    a = inputs.tensor(M, K, 5, 0, "int")
+    b = inputs.tensor(K, N, 5, 1, "int")
+    for relu in (True, False):
+        c, _ = run_gpu(a, b, relu, options=opts)
+        np.testing.assert_array_equal(c.view(np.uint16),
+                                      oracle_ref(a, b, relu)["out16_f32acc"])
+
+
+@pytest.mark.parametrize("case", [
+    dict(lda=1037, ldb=531, ldc=531),             # odd leading dimensions
+    dict(lda=1040, ldb=536, ldc=536),             # padded, 16-byte aligned
+    dict(a_off=1, b_off=3, c_off=5),              # 2-byte-aligned pointers
+    dict(lda=1033, ldb=529, ldc=533, a_off=7, b_off=1, c_off=1),
+])
+def test_strides_and_pointer_offsets(case):
+    M, N, K = 333, 527, 1030
+    a = inputs.tensor(M, K, 9, 0)
+    b = inputs.tensor(K, N, 9, 1)
+    c, pad_ok = run_gpu(a, b, True, **case)
+    assert pad_ok, "wrote outside the M x N region of C"
+    assert_parity(c, oracle_ref(a, b, True), K, True, where=str(case))
+
+
+def test_k_zero_writes_positive_zero():
+    M, N = 37, 45
+    a = np.zeros((M, 0), np.float16)
+    b = np.zeros((0, N), np.float16)
+    c, pad_ok = run_gpu(a, b, True, lda=1, ldb=N)
+    assert pad_ok and (c.view(np.uint16) == 0).all()
+    c, _ = run_gpu(a, b, False, lda=1, ldb=N)
+    assert (c.view(np.uint16) == 0).all()
+
+
+def test_empty_outputs_are_noops():
+    for M, N, K in [(0, 5, 5), (5, 0, 5), (0, 0, 0)]:
+        st = binding.tg_gemm_relu_f16(0, 0, 0, M, N, K, max(K, 1), max(N, 1), max(N, 1), 1, 0)
+        assert st == binding.TG_OK
+
+
+def test_all_negative_products_are_exact_zero():
+    M, N, K = 257, 383, 2000
+    a = np.abs(inputs.tensor(M, K, 13, 0)) + np.float16(0.01)
+    b = -(np.abs(inputs.tensor(K, N, 13, 1)) + np.float16(0.01))
+    for opts in (None, {"split_k": 3}):
+        c, _ = run_gpu(a, b, True, options=opts)
+        assert (c.view(np.uint16) == 0).all()
+        c0, _ = run_gpu(a, b, False, options=opts)
+        assert (c0.view(np.uint16) & 0x8000).all()
+
+
+def test_relu_of_identity_epilogue_and_determinism():
+    M, N, K = 400, 700, 3000
+    a = inputs.tensor(M, K, 17, 0)
+    b = inputs.tensor(K, N, 17, 1)
+    for opts in (None, {"split_k": 5}, {"block_n": 128, "max_ctas": 7}):
+        c1, _ = run_gpu(a, b, True, options=opts)
+        c2, _ = run_gpu(a, b, True, options=opts)
+        np.testing.assert_array_equal(c1.view(np.uint16), c2.view(np.uint16))
+        c0, _ = run_gpu(a, b, False, options=opts)
+        bits = c0.view(np.uint16)
+        np.testing.assert_array_equal(c1.view(np.uint16), np.where(bits & 0x8000, 0, bits))
+
+
+def test_split_k_agrees_with_single_pass():
+    M, N, K = 256, 512, 8192
+    a = inputs.tensor(M, K, 23, 0)
+    b = inputs.tensor(K, N, 23, 1)
+    ref = oracle_ref(a, b, True)
+    for s in (1, 2, 4, 16):
+        c, _ = run_gpu(a, b, True, options={"split_k": s})
+        assert_parity(c, ref, K, True, where=f"split_k={s}")
+
+
+def test_permutation_is_exact():
+    n, N = 300, 700
+    perm = np.random.default_rng(3).permutation(n)
+    P = np.zeros((n, n), np.float16)
+    P[np.arange(n), perm] = 1
+    b = inputs.tensor(n, N, 29, 1)
+    c, _ = run_gpu(P, b, False)
+    np.testing.assert_array_equal(c.view(np.uint16), b[perm].view(np.uint16))
+
+
+def test_subnormal_inputs_are_not_flushed():
+    # products of fp16 subnormals and ones: exact sums in the subnormal range
+    M, N, K = 130, 260, 70
+    a = np.full((M, K), np.float16(2.0 ** -24))
+    a[:, 1::2] = np.float16(3 * 2.0 ** -24)
+    b = np.ones((K, N), np.float16)
+    c, _ = run_gpu(a, b, True)
+    want = oracle_ref(a, b, True)["out16_f32acc"]
+    np.testing.assert_array_equal(c.view(np.uint16), want)
+    assert (want != 0).all()
+
+
+def test_host_buffer_entry_point():
+    M, N, K = 300, 517, 999
+    a = inputs.tensor(M, K, 31, 0)
+    b = inputs.tensor(K, N, 31, 1)
+    from fp16_gemm_relu_gb300 import gemm_relu_host
+
+    c = gemm_relu_host(a, b)
+    assert_parity(c.view(np.uint16), oracle_ref(a, b, True), K, True, where="host entry")
+    # odd host leading dimension on the output
+    out = np.zeros((M, N + 3), np.float16)[:, :N]
+    gemm_relu_host(a, b, out=out)
+    np.testing.assert_array_equal(out.view(np.uint16), c.view(np.uint16))
+
+
+def test_torch_wrapper_and_views():
+    from fp16_gemm_relu_gb300 import gemm_relu
+
+    M, N, K = 200, 300, 400
+    a = inputs.tensor(M, K, 37, 0)
+    b = inputs.tensor(K, N, 37, 1)
+    A = _dev(inputs.embed(a, K + 8))[:, :K]
+    B = _dev(b)
+    C = gemm_relu(A, B)
+    torch.cuda.synchronize()
+    assert_parity(C.cpu().numpy().view(np.uint16), oracle_ref(a, b, True), K, True)
+    with pytest.raises(TypeError):
+        gemm_relu(A.float(), B)
