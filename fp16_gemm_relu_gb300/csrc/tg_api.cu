@@ -413,8 +413,9 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     if (ws)
       cr = encode_ws_3d(enc, &L.out, ws, uint64_t(N), uint64_t(M), uint64_t(P.split_k),
                         uint64_t(pl.ldw));
-    else
-      cr = encode_2d(enc, &L.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C, uint64_t(N), uint64_t(M),
+    else  // a tile store writes whole 16-byte chunks: the map stops at N rounded down to 8
+      cr = encode_2d(enc, &L.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C,
+                     uint64_t(std::max<int64_t>(N & ~int64_t{7}, 8)), uint64_t(M),
                      uint64_t(ldc) * 2, 64, 32);
   }
   if (cr != CUDA_SUCCESS) return fail(cuda_fail(cudaErrorInvalidValue));
@@ -434,6 +435,11 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   gp.debug_flags = o.debug_flags;
   gp.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : kDefaultTimeoutMs);
   gp.err = ds->err;
+  gp.c = static_cast<__half*>(C);
+  gp.ldc = ldc;
+  gp.M = static_cast<int>(M);
+  gp.N = static_cast<int>(N);
+  gp.n_tma = static_cast<int>(N & ~int64_t{7});
   L.grid = P.grid;
   L.stream = stream;
   switch (P.block_n) {

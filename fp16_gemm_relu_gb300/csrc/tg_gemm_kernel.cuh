@@ -56,6 +56,12 @@ struct GemmParams {
   int debug_flags;
   unsigned long long timeout_ns;
   unsigned int* err;
+  // fp16 output only: C itself, for the ragged column tail [n_tma, N) that the TMA store
+  // cannot write (a tile store covers whole 16-byte chunks of a row; the tensor map covers
+  // columns [0, n_tma) with n_tma = N rounded down to a multiple of 8)
+  __half* c;
+  long long ldc;
+  int M, N, n_tma;
 };
 
 template <int BN>
@@ -347,7 +353,8 @@ __device__ __forceinline__ uint32_t relu_pack_h2(uint32_t a, uint32_t b, int rel
 // ---------------------------------------------------------------------------------------
 // tmA:   fp16 A, dims {K, M}, box {64, 128}, 128B swizzle
 // tmB:   fp16 B, dims {N, K}, box {64, 64}, 128B swizzle
-// tmOut: OUT_F32 == false: fp16 C, dims {N, M}, box {64, 32}, 128B swizzle
+// tmOut: OUT_F32 == false: fp16 C, dims {n_tma, M}, box {64, 32}, 128B swizzle (columns
+//        [n_tma, N) are written with plain stores through p.c)
 //        OUT_F32 == true:  f32 workspace, dims {N, M, splits}, box {32, 32, 1}, 128B swizzle
 template <int BN, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -518,21 +525,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.relu);
             pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.relu);
           }
-          uint8_t* st = stg + sb * kStagingBuf;
-          if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
-          __syncwarp();
+          const int col0 = w.n_blk * BN + c * 64;
+          if (col0 < p.n_tma) {
+            uint8_t* st = stg + sb * kStagingBuf;
+            if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+            for (int j = 0; j < 8; ++j) {
+              uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+              *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, smem_u32(st), col0, row0);
+              bulk_commit();
+            }
+            sb ^= 1;
           }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmOut, smem_u32(st), w.n_blk * BN + c * 64, row0);
-            bulk_commit();
+          if (col0 + 64 > p.n_tma && col0 < p.N && row0 + lane < p.M) {
+            // ragged tail columns [n_tma, N): plain 2-byte stores of this thread's row
+            const int jb = max(p.n_tma, col0) - col0;
+            const int je = min(p.N, col0 + 64) - col0;
+            unsigned short* dst = reinterpret_cast<unsigned short*>(p.c) +
+                                  static_cast<long long>(row0 + lane) * p.ldc + col0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (2 * i >= jb && 2 * i < je) dst[2 * i] = static_cast<unsigned short>(pk[i] & 0xFFFFu);
+              if (2 * i + 1 >= jb && 2 * i + 1 < je) dst[2 * i + 1] = static_cast<unsigned short>(pk[i] >> 16);
+            }
           }
-          sb ^= 1;
         }
       } else {
 #pragma unroll 1

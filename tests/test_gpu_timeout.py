@@ -1,0 +1,58 @@
+"""Failure detection without a GPU fault: the first producer of the grid drops one pipeline
+stage (no load, no arrival), so the MMA thread's bounded wait on it runs out.  The kernel must
+record the timeout in the device error word, drain what is in flight, free tensor memory and
+return; the host reads TG_ERR_TIMEOUT; the next call on the same context is correct."""
+
+import numpy as np
+import pytest
+
+import oracle
+from fp16_gemm_relu_gb300 import binding, inputs
+
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def test_dropped_stage_times_out_and_context_survives():
+    from fp16_gemm_relu_gb300 import build
+
+    build.build()
+    torch.cuda.set_device(0)
+    binding.tg_device_error_check(clear=True)
+    M, N, K = 256, 512, 2048
+    a = inputs.tensor(M, K, 3, 0)
+    b = inputs.tensor(K, N, 3, 1)
+    A = torch.from_numpy(a).cuda()
+    B = torch.from_numpy(b).cuda()
+    C = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    opts = {"debug_flags": binding.TG_DEBUG_DROP_FIRST_STAGE, "timeout_ms": 200}
+    st = binding.tg_gemm_relu_f16_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, K, N, N,
+                                     1, opts, s)
+    assert st == binding.TG_OK  # queued; the failure is only visible after it ran
+    st, word = binding.tg_device_error_check(clear=True)
+    assert st == binding.TG_ERR_TIMEOUT
+    assert word & 1 and ((word >> 8) & 0xFF) in (1, 2, 3)
+    # the context is still usable and the error word was cleared
+    st, word = binding.tg_device_error_check(clear=False)
+    assert st == binding.TG_OK and word == 0
+    st = binding.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, K, N, N, 1, s)
+    assert st == binding.TG_OK
+    torch.cuda.synchronize()
+    ref = oracle.gemm_relu(a, b, relu=True)
+    assert_parity(C.cpu().numpy().view(np.uint16), ref, K, True, where="after timeout")
+    st, word = binding.tg_device_error_check(clear=True)
+    assert st == binding.TG_OK and word == 0
+
+
+def test_host_entry_reports_clean_status():
+    M, N, K = 64, 64, 64
+    a = inputs.tensor(M, K, 4, 0)
+    b = inputs.tensor(K, N, 4, 1)
+    out = np.empty((M, N), np.float16)
+    st = binding.tg_gemm_relu_f16_host(a.ctypes.data, b.ctypes.data, out.ctypes.data, M, N, K,
+                                       K, N, N, 1, 0)
+    assert st == binding.TG_OK
