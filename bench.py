@@ -191,9 +191,12 @@ def cpu_baseline(wl, a, b, target_s: float, relu=True):
     """The oracle as it stands, on a bounded sample: the first R rows of C."""
     import oracle
 
-    dt, flops, threads = oracle.timed_rows(a, b, 2, relu=relu)  # calibration
-    per_row = dt / 2
-    rows = int(max(1, min(wl.M, target_s / max(per_row, 1e-6))))
+    # calibrate: each call has a fixed cost (decoding B) plus a cost per row of C
+    t1, _, _ = oracle.timed_rows(a, b, 4, relu=relu)
+    t2, _, _ = oracle.timed_rows(a, b, 12, relu=relu)
+    per_row = max((t2 - t1) / 8, 1e-6)
+    fixed = max(t1 - 4 * per_row, 0.0)
+    rows = int(max(1, min(wl.M, (target_s - fixed) / per_row)))
     dt, flops, threads = oracle.timed_rows(a, b, rows, relu=relu)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"first {rows} of {wl.M} rows of C ({rows}x{wl.N}x{wl.K}), float32 "
