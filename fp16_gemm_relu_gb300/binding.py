@@ -82,6 +82,7 @@ def load_library() -> ctypes.CDLL:
         L.tg_gemm_relu_f16.argtypes = gemm_args + [vp]
         L.tg_gemm_relu_f16_ex.argtypes = gemm_args + [ctypes.POINTER(tg_options), vp]
         L.tg_gemm_relu_f16_host.argtypes = gemm_args + [vp]
+        L.tg_gemm_relu_f16_splitk_noalloc.argtypes = gemm_args + [ci, vp]
         L.tg_plan_query.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, ci,
                                     ctypes.POINTER(tg_options), ctypes.POINTER(tg_plan)]
         L.tg_device_error_check.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
@@ -91,6 +92,7 @@ def load_library() -> ctypes.CDLL:
         L.tg_release_workspace.argtypes = []
         L.tg_version.argtypes = []
         for name in ("tg_gemm_relu_f16", "tg_gemm_relu_f16_ex", "tg_gemm_relu_f16_host",
+                     "tg_gemm_relu_f16_splitk_noalloc",
                      "tg_plan_query", "tg_device_error_check", "tg_last_cuda_error",
                      "tg_release_workspace", "tg_version"):
             getattr(L, name).restype = ci
@@ -129,6 +131,19 @@ def tg_gemm_relu_f16_host(hA: int, hB: int, hC: int, M: int, N: int, K: int, lda
                           ldb: int, ldc: int, epilogue_flag: int, stream: int = 0) -> int:
     return load_library().tg_gemm_relu_f16_host(hA, hB, hC, M, N, K, lda, ldb, ldc,
                                                 epilogue_flag, stream or None)
+
+
+def tg_gemm_relu_f16_splitk_noalloc(A: int, B: int, C: int, M: int, N: int, K: int, lda: int,
+                                    ldb: int, ldc: int, epilogue_flag: int, split_k: int = 0,
+                                    stream: int = 0) -> int:
+    """Split-K GEMM whose float32 workspace is a fixed array inside the library, for callers
+    that must not allocate device memory during the call (limits in the C header)."""
+    return load_library().tg_gemm_relu_f16_splitk_noalloc(A, B, C, M, N, K, lda, ldb, ldc,
+                                                          epilogue_flag, split_k,
+                                                          stream or None)
+
+
+TG_STATIC_WORKSPACE_BYTES = 64 << 20
 
 
 def tg_plan_query(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int, ldc: int,

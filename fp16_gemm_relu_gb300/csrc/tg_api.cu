@@ -461,6 +461,21 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 }  // namespace
 
 namespace tg {
+// Hooks for other translation units of this library (not part of the C ABI).
+cudaError_t error_word_address(unsigned int** out) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_tg_error_word);
+}
+
+bool tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) { return encode_fn(fn) == TG_OK; }
+
+cudaError_t launch_splitk_reduce(const float* ws, int64_t ldw, int64_t split_stride, int splits,
+                                 void* C, int64_t ldc, int64_t M, int64_t N, int relu,
+                                 int num_sms, cudaStream_t stream) {
+  tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), num_sms), 256, 0, stream>>>(
+      ws, ldw, split_stride, splits, static_cast<__half*>(C), ldc, M, N, relu);
+  return cudaGetLastError();
+}
+
 int gemm_stages(int block_n) {
   switch (block_n) {
     case 256: return TileCfg<256>::kStages;

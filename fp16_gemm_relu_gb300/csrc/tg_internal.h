@@ -2,7 +2,9 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "tg_gemm_kernel.cuh"
 
@@ -23,5 +25,16 @@ int gemm_stages(int block_n);
 cudaError_t launch_gemm_bn256(const GemmLaunch& l, bool out_f32);
 cudaError_t launch_gemm_bn192(const GemmLaunch& l, bool out_f32);
 cudaError_t launch_gemm_bn128(const GemmLaunch& l, bool out_f32);
+
+// Address of the device error word that kernels set when a pipeline wait runs out.
+cudaError_t error_word_address(unsigned int** out);
+
+// cuTensorMapEncodeTiled from the driver (false if the driver does not provide it).
+bool tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn);
+
+// Deterministic split-K reduction: C = fp16(epi(sum_s W[s])) (see tg_splitk_reduce_kernel).
+cudaError_t launch_splitk_reduce(const float* ws, int64_t ldw, int64_t split_stride, int splits,
+                                 void* C, int64_t ldc, int64_t M, int64_t N, int relu,
+                                 int num_sms, cudaStream_t stream);
 
 }  // namespace tg

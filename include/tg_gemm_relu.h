@@ -138,6 +138,37 @@ tg_status tg_last_cuda_error(int* cuda_err);
 /* Returns the library pool's unused scratch memory on the current device to the system. */
 tg_status tg_release_workspace(void);
 
+/*
+ * Split-K relu(A·B) that allocates no memory at all.  The paper has no counterpart to it: it
+ * exists for callers that cannot call cudaMalloc, cudaMallocAsync or any other allocator
+ * while they run a GEMM, for example code running inside an allocator that must not be
+ * re-entered, a runtime that has handed all device memory to its own arena, or
+ * latency-critical work where an allocation could block or fail.
+ *
+ * It always takes the split-K path: `split_k` splits (clamped to 1..number of 64-wide K
+ * blocks; 0 picks 2) each write a float32 partial tile into a fixed workspace, and a second
+ * kernel adds the splits in order, applies the epilogue and writes fp16 C.  The workspace is
+ * one array of TG_STATIC_WORKSPACE_BYTES bytes of device memory that is part of the library
+ * itself: every GPU on which the library is used holds it until the process exits.
+ *
+ *  - Needs split_k * M * (N rounded up to 4) * 4 bytes <= TG_STATIC_WORKSPACE_BYTES;
+ *    larger problems return TG_ERR_NO_WORKSPACE before anything is launched.
+ *  - A and B must be 16-byte aligned with lda and ldb multiples of 8 (TG_ERR_MISALIGNED
+ *    otherwise); C only needs 2-byte alignment.  Other arguments as for tg_gemm_relu_f16.
+ *  - The first call on each device does a one-time set-up with that device current (it
+ *    looks up the workspace's device address and the device's properties); make that first
+ *    call before any stream capture.
+ *  - All calls share the one workspace, and it keeps whatever the last call left there.
+ *    Nothing in it needs to start at zero (each split overwrites its whole slice before the
+ *    reduction reads it), but calls whose work overlaps on the GPU race on it: issue them
+ *    on one stream, or order them with events.
+ */
+#define TG_STATIC_WORKSPACE_BYTES (64ull << 20)
+tg_status tg_gemm_relu_f16_splitk_noalloc(const void* A, const void* B, void* C, int64_t M,
+                                          int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                          int64_t ldc, int epilogue_flag, int split_k,
+                                          tg_stream_t stream);
+
 /* Library version as major*10000 + minor*100 + patch. */
 int tg_version(void);
 
