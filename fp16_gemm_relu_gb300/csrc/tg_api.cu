@@ -38,6 +38,7 @@ struct DeviceState {
   int sm_count = 0;
   cudaMemPool_t pool = nullptr;
   unsigned int* err = nullptr;
+  int pair_clusters = 0;  // co-resident clusters of the CTA-pair kernel (0: do not use it)
 };
 
 constexpr int kMaxDevices = 64;
@@ -72,6 +73,12 @@ tg_status current_device(DeviceState** out) {
       if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&s.err), g_tg_error_word)) != cudaSuccess)
         return cuda_fail(e);
       s.sm_count = sms;
+      int clusters = 0;
+      if (tg::gemm_pair_max_clusters(&clusters) != cudaSuccess) {
+        clusters = 0;
+        cudaGetLastError();  // a failed occupancy query only disables the pair kernel
+      }
+      s.pair_clusters = clusters;
       s.status = TG_OK;
     }
     s.ready = true;
@@ -140,16 +147,18 @@ double kblock_cycles(int bn) {
 // memory time = the algorithmic bytes at 6.8 TB/s, inflated when a wave keeps fewer than
 // 60% of the SMs busy; plus the float32 workspace traffic of split-K and its extra launch.
 tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N, int64_t K,
-                    int64_t lda, int64_t ldb, int64_t ldc, int num_sms, const tg_options* opt,
-                    Plan* out) {
+                    int64_t lda, int64_t ldb, int64_t ldc, int num_sms, int pair_clusters,
+                    const tg_options* opt, Plan* out) {
   tg_options o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
   if (num_sms <= 0) return TG_ERR_INVALID_ARG;
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 192 && o.block_n != 256)
     return TG_ERR_INVALID_ARG;
-  if (o.split_k < 0 || o.panel_m < 0 || o.max_ctas < 0 || o.timeout_ms < 0)
+  if (o.split_k < 0 || o.panel_m < 0 || o.max_ctas < 0 || o.timeout_ms < 0 || o.pair < -1 ||
+      o.pair > 1)
     return TG_ERR_INVALID_ARG;
+  if (o.pair == 1 && o.block_n != 0 && o.block_n != 256) return TG_ERR_INVALID_ARG;
 
   Plan pl;
   std::memset(&pl, 0, sizeof(pl));
@@ -176,13 +185,21 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
 
   struct Cand {
     double t;
-    int bn, s, active;
+    int bn, s, active, pair;
   };
-  Cand cands[3 * 32];
+  Cand cands[4 * 32];
   int nc = 0;
-  for (int bn : kBlockNs) {
+  // tile kinds: the 256x256 CTA-pair tile, then single-CTA 128 x {256, 192, 128}
+  const int pair_cap = std::min(o.max_ctas > 0 ? o.max_ctas / 2 : num_sms / 2,
+                                pair_clusters > 0 ? pair_clusters : num_sms / 2);
+  for (int kind = 0; kind < 4; ++kind) {
+    const int pair = kind == 0 ? 1 : 0;
+    const int bn = pair ? 256 : kBlockNs[kind - 1];
+    if (pair && (o.pair < 0 || pair_cap < 1)) continue;
+    if (!pair && o.pair > 0) continue;
     if (o.block_n && bn != o.block_n) continue;
-    const int64_t tiles = P.tiles_m * cdiv(N, bn);
+    const int bm = pair ? 2 * tg::kBM : tg::kBM;
+    const int64_t tiles = cdiv(M, bm) * cdiv(N, bn);
     const int64_t s_max = o.split_k ? std::min<int64_t>(o.split_k, P.kblocks)
                                     : std::min<int64_t>(P.kblocks, 32);
     const int64_t s_min = o.split_k ? s_max : 1;
@@ -191,20 +208,24 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
       const int64_t s_eff = cdiv(P.kblocks, kbps);
       if (!o.split_k && s_eff != s) continue;  // same plan as a smaller s
       const int64_t units = tiles * s_eff;
-      const int64_t grid = std::min<int64_t>(units, grid_cap);
+      // a pair unit occupies two SMs; the per-SM k-block cost of the pair tile is the MMA
+      // time alone (each SM loads 32 KB per k-block, well under the L2 budget)
+      const int64_t slots_cap = pair ? pair_cap : grid_cap;
+      const int64_t grid = std::min<int64_t>(units, slots_cap);
       const int64_t waves = cdiv(units, grid);
       const bool ws = s_eff > 1 || !c_direct;
-      const double t_mma = double(waves) * double(kbps) * kblock_cycles(bn) / clk;
+      const double kb_cycles = pair ? 512.0 : kblock_cycles(bn);
+      const double t_mma = double(waves) * double(kbps) * kb_cycles / clk;
       double slots = 0.0;  // wave-by-wave occupancy penalty on the memory time
       for (int64_t wv = 0; wv < waves; ++wv) {
-        const int64_t active = std::min<int64_t>(grid, units - wv * grid);
+        const int64_t active = (pair ? 2 : 1) * std::min<int64_t>(grid, units - wv * grid);
         slots += std::max<double>(double(active), 0.6 * num_sms);
       }
-      const double t_hbm = alg_bytes / hbm * (slots / double(units));
+      const double t_hbm = alg_bytes / hbm * (slots / double((pair ? 2 : 1) * units));
       // workspace traffic plus the extra launch of the reduction kernel (~3 us)
       const double t_ws = ws ? (2.0 * 4.0 * double(s_eff) * M * N + 2.0 * M * N) / hbm + 3e-6 : 0.0;
       cands[nc++] = Cand{std::max(t_mma, t_hbm) + t_ws, bn, static_cast<int>(s_eff),
-                         static_cast<int>(grid)};
+                         static_cast<int>((pair ? 2 : 1) * grid), pair};
     }
   }
   if (nc == 0) return TG_ERR_INVALID_ARG;
@@ -218,13 +239,19 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   }
   const int best_bn = cands[pick].bn;
   const int best_s = cands[pick].s;
+  const int best_pair = cands[pick].pair;
+  P.cta_pair = best_pair;
+  P.block_m = best_pair ? 2 * tg::kBM : tg::kBM;
   P.block_n = best_bn;
-  P.stages = tg::gemm_stages(best_bn);
+  P.stages = best_pair ? tg::PairCfg::kStages : tg::gemm_stages(best_bn);
   P.kblocks_per_split = cdiv(P.kblocks, best_s);
   P.split_k = static_cast<int>(cdiv(P.kblocks, P.kblocks_per_split));
+  P.tiles_m = cdiv(M, P.block_m);
   P.tiles_n = cdiv(N, best_bn);
   P.units = P.tiles_m * P.tiles_n * P.split_k;
-  P.grid = static_cast<int>(std::min<int64_t>(P.units, grid_cap));
+  if (P.units >= (int64_t{1} << 31)) return TG_ERR_INVALID_ARG;
+  P.grid = best_pair ? 2 * static_cast<int>(std::min<int64_t>(P.units, pair_cap))
+                     : static_cast<int>(std::min<int64_t>(P.units, grid_cap));
   P.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : kDefaultPanel, P.tiles_m));
   P.workspace_epilogue = (P.split_k > 1 || !c_direct) ? 1 : 0;
 
@@ -361,7 +388,8 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   }
   Plan pl;
   st = make_plan(reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
-                 reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, ds->sm_count, opt, &pl);
+                 reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, ds->sm_count,
+                 ds->pair_clusters, opt, &pl);
   if (st != TG_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if ((st = encode_fn(&enc)) != TG_OK) return st;
@@ -442,7 +470,9 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   gp.n_tma = static_cast<int>(N & ~int64_t{7});
   L.grid = P.grid;
   L.stream = stream;
-  switch (P.block_n) {
+  if (P.cta_pair) {
+    e = tg::launch_gemm_pair(L, ws != nullptr);
+  } else switch (P.block_n) {
     case 256: e = tg::launch_gemm_bn256(L, ws != nullptr); break;
     case 192: e = tg::launch_gemm_bn192(L, ws != nullptr); break;
     default: e = tg::launch_gemm_bn128(L, ws != nullptr); break;
@@ -517,7 +547,7 @@ tg_status tg_plan_query(const void* A, const void* B, const void* C, int64_t M, 
   if (st != TG_OK) return st;
   Plan pl;
   st = make_plan(reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
-                 reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, num_sms, opt, &pl);
+                 reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, num_sms, 0, opt, &pl);
   if (st == TG_OK) *out = pl.pub;
   return st;
 }

@@ -170,6 +170,87 @@ __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- clusters of two CTAs (the CTA pair of tcgen05 cta_group::2) ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// every thread of both CTAs; release/acquire orders shared-memory work across the cluster
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion is signalled on an mbarrier that
+// may live in the peer CTA of the pair (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t holder_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   holder_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 256 x N x 16 MMA over the CTA pair: A rows 0-127 from this CTA's shared memory and 128-255
+// from the peer's (same offset), B columns split in halves the same way; D lanes in each
+// CTA's TMEM hold that CTA's 128 rows.
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the barrier at this shared-memory offset in every CTA of `mask` when the
+// pair MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_alloc(uint32_t holder_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    holder_smem),
@@ -348,6 +429,98 @@ __device__ __forceinline__ uint32_t relu_pack_h2(uint32_t a, uint32_t b, int rel
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// One output tile's epilogue for one warp: TMEM lane quarter at `tl` (32 rows starting at
+// row0, BN columns starting at col_base) -> registers -> epilogue -> 128B-swizzled staging ->
+// TMA store.  After the last tcgen05.ld the warp releases the accumulator by arriving on
+// `release_bar` (a CTA-local barrier, or with `remote` a shared::cluster address of the
+// barrier in another CTA of the cluster).
+template <int BN, bool OUT_F32>
+__device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const GemmParams& p,
+                                              uint32_t tl, int row0, int col_base, int split,
+                                              uint8_t* stg, int& sb, uint32_t release_bar,
+                                              bool remote, int lane) {
+  auto release = [&]() {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      if (remote)
+        mbar_arrive_cluster(release_bar);
+      else
+        mbar_arrive(release_bar);
+    }
+  };
+  if constexpr (!OUT_F32) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 64; ++c) {
+      uint32_t r0[32], r1[32];
+      tmem_ld_x32(tl + c * 64, r0);
+      tmem_wait_ld(r0);
+      tmem_ld_x32(tl + c * 64 + 32, r1);
+      tmem_wait_ld(r1);
+      if (c == BN / 64 - 1) release();
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.relu);
+        pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.relu);
+      }
+      const int col0 = col_base + c * 64;
+      if (col0 < p.n_tma) {
+        uint8_t* st = stg + sb * kStagingBuf;
+        if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmOut, smem_u32(st), col0, row0);
+          bulk_commit();
+        }
+        sb ^= 1;
+      }
+      if (col0 + 64 > p.n_tma && col0 < p.N && row0 + lane < p.M) {
+        // ragged tail columns [n_tma, N): plain 2-byte stores of this thread's row
+        const int jb = max(p.n_tma, col0) - col0;
+        const int je = min(p.N, col0 + 64) - col0;
+        unsigned short* dst = reinterpret_cast<unsigned short*>(p.c) +
+                              static_cast<long long>(row0 + lane) * p.ldc + col0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (2 * i >= jb && 2 * i < je) dst[2 * i] = static_cast<unsigned short>(pk[i] & 0xFFFFu);
+          if (2 * i + 1 >= jb && 2 * i + 1 < je) dst[2 * i + 1] = static_cast<unsigned short>(pk[i] >> 16);
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_x32(tl + c * 32, r);
+      tmem_wait_ld(r);
+      if (c == BN / 32 - 1) release();
+      uint8_t* st = stg + sb * kStagingBuf;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint4 v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmOut, smem_u32(st), col_base + c * 32, row0, split);
+        bulk_commit();
+      }
+      sb ^= 1;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------------------
@@ -505,85 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * Cfg::kAccStride);
-      const int row0 = w.m_blk * kBM + q * 32;
-      if constexpr (!OUT_F32) {
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_x32(tl + c * 64, r0);
-          tmem_wait_ld(r0);
-          tmem_ld_x32(tl + c * 64 + 32, r1);
-          tmem_wait_ld(r1);
-          if (c == BN / 64 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
-          }
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.relu);
-            pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.relu);
-          }
-          const int col0 = w.n_blk * BN + c * 64;
-          if (col0 < p.n_tma) {
-            uint8_t* st = stg + sb * kStagingBuf;
-            if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-              *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmOut, smem_u32(st), col0, row0);
-              bulk_commit();
-            }
-            sb ^= 1;
-          }
-          if (col0 + 64 > p.n_tma && col0 < p.N && row0 + lane < p.M) {
-            // ragged tail columns [n_tma, N): plain 2-byte stores of this thread's row
-            const int jb = max(p.n_tma, col0) - col0;
-            const int je = min(p.N, col0 + 64) - col0;
-            unsigned short* dst = reinterpret_cast<unsigned short*>(p.c) +
-                                  static_cast<long long>(row0 + lane) * p.ldc + col0;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (2 * i >= jb && 2 * i < je) dst[2 * i] = static_cast<unsigned short>(pk[i] & 0xFFFFu);
-              if (2 * i + 1 >= jb && 2 * i + 1 < je) dst[2 * i + 1] = static_cast<unsigned short>(pk[i] >> 16);
-            }
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld_x32(tl + c * 32, r);
-          tmem_wait_ld(r);
-          if (c == BN / 32 - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
-          }
-          uint8_t* st = stg + sb * kStagingBuf;
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint4 v = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-            *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmOut, smem_u32(st), w.n_blk * BN + c * 32, row0, w.split);
-            bulk_commit();
-          }
-          sb ^= 1;
-        }
-      }
+      epilogue_tile<BN, OUT_F32>(&tmOut, p, tl, w.m_blk * kBM + q * 32, w.n_blk * BN, w.split,
+                                 stg, sb, smem_u32(&tempty[buf]), false, lane);
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
@@ -595,6 +691,211 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// The CTA-pair kernel: 256 x 256 output tiles computed by a cluster of two CTAs with
+// tcgen05.mma.cta_group::2.  CTA r of the pair loads A rows [256m + 128r, +128) and B
+// columns [256n + 128r, +128) of each k-block into its own shared memory; both CTAs' TMA
+// loads signal the leader's (r = 0) full barrier; the leader alone issues the MMAs, which
+// read both CTAs' tiles and accumulate rows [128r, +128) of the 256 x 256 tile into CTA r's
+// TMEM.  The leader's tcgen05.commit multicasts to both CTAs' empty (stage free) and
+// tmem-full barriers; both CTAs' epilogue warps release an accumulator by arriving on the
+// leader's tmem-empty barrier.  Per SM and k-block this moves 32 KB (16 KB A + 16 KB B)
+// from L2 instead of the 48 KB of the single-CTA 128 x 256 tile, for the same MMA work.
+// ---------------------------------------------------------------------------------------
+struct PairCfg {
+  static constexpr int kBN = 256;                       // N of the pair tile
+  static constexpr int kHalfN = 128;                    // B columns in each CTA
+  static constexpr int kAStage = kBM * kBK * 2;         // 16 KB
+  static constexpr int kBBox = kBK * 64 * 2;            // 8 KB
+  static constexpr int kBStage = kBK * kHalfN * 2;      // 16 KB
+  static constexpr int kStageBytes = kAStage + kBStage; // 32 KB per CTA
+  static constexpr int kStagingBytes = kEpiWarps * 2 * kStagingBuf;
+  static constexpr int kStagesFit = (kSmemLimit - kSmemReserve - kStagingBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kAccStride = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes + kStagingBytes;
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
+};
+
+// Same maps as tg_gemm_tc_kernel; tiles_m/tiles_n in p count 256 x 256 pair tiles.
+template <bool OUT_F32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  using Cfg = PairCfg;
+  constexpr int S = Cfg::kStages;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * Cfg::kAStage;
+  uint8_t* sStg = sB + S * Cfg::kBStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStagingBytes);
+  uint64_t* full = bars;        // used in the leader
+  uint64_t* empty = bars + S;   // in both CTAs
+  uint64_t* tfull = bars + 2 * S;
+  uint64_t* tempty = tfull + 2; // used in the leader
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer (both CTAs) ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      bool dropped = false;
+      for (int u = cluster; u < p.units; u += nclusters) {
+        const Unit w = unit_of(p, u);
+        const int arow = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM;
+        const int bcol = w.n_blk * Cfg::kBN + static_cast<int>(rank) * Cfg::kHalfN;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
+            goto pair_producer_done;
+          if ((p.debug_flags & kDebugDropFirstStage) && cluster == 0 && rank == 0 && !dropped) {
+            dropped = true;  // injected fault: the leader never arms this stage
+          } else {
+            const uint32_t fb_local = smem_u32(&full[stage]);
+            const uint32_t fb = mapa_shared(fb_local, 0);
+            if (rank == 0) {
+              mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
+              armed |= 1u << stage;
+              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            }
+            tma_load_2d_pair(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, arow);
+#pragma unroll
+            for (int j = 0; j < Cfg::kHalfN / 64; ++j)
+              tma_load_2d_pair(smem_u32(sB + stage * Cfg::kBStage + j * Cfg::kBBox), &tmB, fb,
+                               bcol + j * 64, kb * kBK);
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    pair_producer_done:
+      // the leader's full barriers count both CTAs' bytes: once they completed, no load of
+      // either CTA is still writing shared memory
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) wait_phase_drain(smem_u32(&full[s]), (armed_parity >> s) & 1u, p);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer (leader) ------------------------------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      for (int u = cluster; u < p.units; u += nclusters, ++t) {
+        const Unit w = unit_of(p, u);
+        const int buf = t & 1;
+        const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+        if (!wait_phase(smem_u32(&tempty[buf]), use ^ 1u, abort_flag, p, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        bool ok = true;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&full[stage]), phase, abort_flag, p, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_a_kmajor(smem_u32(sA + stage * Cfg::kAStage));
+          const uint64_t bd = desc_b_mnmajor(smem_u32(sB + stage * Cfg::kBStage));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16_pair(d_tmem, ad + static_cast<uint64_t>(2 * k),
+                          bd + static_cast<uint64_t>(128 * k), idesc,
+                          (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          umma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(smem_u32(&tfull[buf]), 0x3);
+      }
+      umma_commit_pair(smem_u32(drain));
+      wait_phase_drain(smem_u32(drain), 0u, p);
+    }
+  } else {
+    // ------------------------------ epilogue (both CTAs) ------------------------------
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    uint8_t* stg = sStg + ew * 2 * kStagingBuf;
+    int sb = 0;
+    int t = 0;
+    for (int u = cluster; u < p.units; u += nclusters, ++t) {
+      const Unit w = unit_of(p, u);
+      const int buf = t & 1;
+      const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const int row0 = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;
+      epilogue_tile<Cfg::kBN, OUT_F32>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, w.split, stg,
+                                       sb, mapa_shared(smem_u32(&tempty[buf]), 0), true, lane);
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+
+  // After an abort the follower cannot observe its own loads (they complete on the leader's
+  // barriers): give any that are still in flight time to land before the CTA can exit.
+  if (rank != 0 && *abort_flag && threadIdx.x == 0) __nanosleep(200000);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // all MMAs into either CTA's TMEM and all remote arrivals are done
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
   }
 }
 

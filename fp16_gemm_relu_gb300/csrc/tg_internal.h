@@ -26,6 +26,11 @@ cudaError_t launch_gemm_bn256(const GemmLaunch& l, bool out_f32);
 cudaError_t launch_gemm_bn192(const GemmLaunch& l, bool out_f32);
 cudaError_t launch_gemm_bn128(const GemmLaunch& l, bool out_f32);
 
+// CTA-pair kernel (256 x 256 tiles; l.grid must be even, l.p counts pair tiles).
+cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32);
+// Clusters of two that can be resident at once on the current device.
+cudaError_t gemm_pair_max_clusters(int* out);
+
 // Address of the device error word that kernels set when a pipeline wait runs out.
 cudaError_t error_word_address(unsigned int** out);
 

@@ -72,6 +72,7 @@ typedef struct {
   int max_ctas;         /* 0 (one per SM), or a cap on the persistent grid */
   int debug_flags;      /* TG_DEBUG_* below; 0 in normal use */
   int timeout_ms;       /* 0 (default 2000 ms), or the per-wait limit of the pipeline */
+  int pair;             /* 0: choose; 1: use the two-CTA 256x256 tile; -1: never use it */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
@@ -93,6 +94,7 @@ typedef struct {
   int workspace_epilogue;      /* C produced by the float32 scratch + conversion pass */
   int64_t workspace_bytes;     /* scratch needed per call */
   int kernels;                 /* kernel launches per call */
+  int cta_pair;                /* 1: 256x256 tiles on clusters of two CTAs (tcgen05 cta_group::2) */
 } tg_plan;
 
 /*

@@ -72,12 +72,24 @@ def _plan(M, N, K, **kw):
     return tg.plan(M, N, K, options=opts, **kw)
 
 
-def test_plan_square_is_one_kernel_wide_tiles(lib):
+def test_plan_square_is_one_kernel_pair_tiles(lib):
     p = _plan(8192, 8192, 8192)
-    assert (p["block_m"], p["block_n"], p["block_k"]) == (128, 256, 64)
+    assert p["cta_pair"] == 1
+    assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 64)
     assert p["split_k"] == 1 and p["kernels"] == 1 and p["workspace_bytes"] == 0
-    assert p["tiles_m"] == 64 and p["tiles_n"] == 32 and p["units"] == 2048
-    assert p["grid"] == 152 and p["stages"] == 4
+    assert p["tiles_m"] == 32 and p["tiles_n"] == 32 and p["units"] == 1024
+    assert p["grid"] == 152 and p["grid"] % 2 == 0 and p["stages"] == 6
+    q = _plan(8192, 8192, 8192, options={"pair": -1})
+    assert q["cta_pair"] == 0 and (q["block_m"], q["block_n"]) == (128, 256)
+    assert q["units"] == 2048 and q["grid"] == 152 and q["stages"] == 4
+
+
+def test_plan_pair_overrides(lib):
+    p = _plan(300, 600, 1500, options={"pair": 1, "max_ctas": 5})
+    assert p["cta_pair"] == 1 and p["grid"] == 4 and p["tiles_m"] == 2 and p["tiles_n"] == 3
+    st, _ = binding.tg_plan_query(4096, 4096, 4096, 64, 64, 64, 64, 64, 64, 152,
+                                  {"pair": 1, "block_n": 128})
+    assert st == binding.TG_ERR_INVALID_ARG
 
 
 def test_plan_skinny_fills_the_machine(lib):
@@ -107,7 +119,7 @@ def test_plan_alignment_from_pointers(lib):
 
 def test_plan_overrides(lib):
     p = _plan(1000, 1000, 1000, options={"block_n": 128, "split_k": 3, "max_ctas": 5,
-                                          "panel_m": 2})
+                                          "panel_m": 2, "pair": -1})
     assert p["block_n"] == 128 and p["split_k"] == 3 and p["grid"] == 5 and p["panel_m"] == 2
     assert p["workspace_epilogue"] == 1 and p["units"] == 8 * 8 * 3
     # more splits than K blocks are clamped, and no split is empty

@@ -91,6 +91,9 @@ FORCED = [
     {"force_repack": 1}, {"force_workspace": 1},
     {"max_ctas": 1}, {"max_ctas": 3, "split_k": 2}, {"max_ctas": 5, "panel_m": 1},
     {"max_ctas": 2, "block_n": 128, "panel_m": 2},
+    {"pair": 1}, {"pair": 1, "split_k": 3}, {"pair": 1, "max_ctas": 2},
+    {"pair": 1, "max_ctas": 6, "panel_m": 1}, {"pair": 1, "force_repack": 1},
+    {"pair": 1, "force_workspace": 1}, {"pair": -1},
 ]
 
 
@@ -104,8 +107,9 @@ def test_forced_plans_parity(opts):
     assert_parity(c, oracle_ref(a, b, True), K, True, where=str(opts))
 
 
-@pytest.mark.parametrize("opts", [None, {"split_k": 4}, {"max_ctas": 3}, {"force_repack": 1,
-                                                                            "split_k": 3}])
+@pytest.mark.parametrize("opts", [None, {"split_k": 4}, {"max_ctas": 3},
+                                  {"force_repack": 1, "split_k": 3}, {"pair": 1},
+                                  {"pair": 1, "split_k": 5, "max_ctas": 4}])
 @pytest.mark.parametrize("M,N,K", [(200, 300, 700), (129, 65, 4099)])
 def test_integer_inputs_bitwise(opts, M, N, K):
     a = inputs.tensor(M, K, 5, 0, "int")
@@ -122,13 +126,14 @@ def test_integer_inputs_bitwise(opts, M, N, K):
     dict(a_off=1, b_off=3, c_off=5),              # 2-byte-aligned pointers
     dict(lda=1033, ldb=529, ldc=533, a_off=7, b_off=1, c_off=1),
 ])
-def test_strides_and_pointer_offsets(case):
+@pytest.mark.parametrize("pair", [-1, 1])
+def test_strides_and_pointer_offsets(case, pair):
     M, N, K = 333, 527, 1030
     a = inputs.tensor(M, K, 9, 0)
     b = inputs.tensor(K, N, 9, 1)
-    c, pad_ok = run_gpu(a, b, True, **case)
+    c, pad_ok = run_gpu(a, b, True, options={"pair": pair}, **case)
     assert pad_ok, "wrote outside the M x N region of C"
-    assert_parity(c, oracle_ref(a, b, True), K, True, where=str(case))
+    assert_parity(c, oracle_ref(a, b, True), K, True, where=f"{case} pair={pair}")
 
 
 def test_k_zero_writes_positive_zero():
@@ -162,7 +167,8 @@ def test_relu_of_identity_epilogue_and_determinism():
     M, N, K = 400, 700, 3000
     a = inputs.tensor(M, K, 17, 0)
     b = inputs.tensor(K, N, 17, 1)
-    for opts in (None, {"split_k": 5}, {"block_n": 128, "max_ctas": 7}):
+    for opts in (None, {"split_k": 5}, {"block_n": 128, "max_ctas": 7}, {"pair": 1},
+                 {"pair": 1, "split_k": 3, "max_ctas": 4}):
         c1, _ = run_gpu(a, b, True, options=opts)
         c2, _ = run_gpu(a, b, True, options=opts)
         np.testing.assert_array_equal(c1.view(np.uint16), c2.view(np.uint16))
@@ -177,8 +183,9 @@ def test_split_k_agrees_with_single_pass():
     b = inputs.tensor(K, N, 23, 1)
     ref = oracle_ref(a, b, True)
     for s in (1, 2, 4, 16):
-        c, _ = run_gpu(a, b, True, options={"split_k": s})
-        assert_parity(c, ref, K, True, where=f"split_k={s}")
+        for pair in (-1, 1):
+            c, _ = run_gpu(a, b, True, options={"split_k": s, "pair": pair})
+            assert_parity(c, ref, K, True, where=f"split_k={s} pair={pair}")
 
 
 def test_permutation_is_exact():

@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 
-def test_dropped_stage_times_out_and_context_survives():
+@pytest.mark.parametrize("pair", [-1, 1], ids=["single_cta", "cta_pair"])
+def test_dropped_stage_times_out_and_context_survives(pair):
     from fp16_gemm_relu_gb300 import build
 
     build.build()
@@ -29,7 +30,7 @@ def test_dropped_stage_times_out_and_context_survives():
     B = torch.from_numpy(b).cuda()
     C = torch.zeros((M, N), dtype=torch.float16, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
-    opts = {"debug_flags": binding.TG_DEBUG_DROP_FIRST_STAGE, "timeout_ms": 200}
+    opts = {"debug_flags": binding.TG_DEBUG_DROP_FIRST_STAGE, "timeout_ms": 200, "pair": pair}
     st = binding.tg_gemm_relu_f16_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, K, N, N,
                                      1, opts, s)
     assert st == binding.TG_OK  # queued; the failure is only visible after it ran
