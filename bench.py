@@ -43,6 +43,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="square8192", choices=workloads.ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--epilogue", default="relu", choices=["relu", "bias_gelu", "bias_relu_residual"],
+                    help="relu: the metric's path; the others time the fused bias/GELU/residual "
+                         "epilogue on the same GEMM")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -275,11 +278,29 @@ def run_ours(args, wl):
     handle = stream.cuda_stream
     lib = binding.load_library()
 
-    def step():
-        st = lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
-                                  wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU, handle)
-        if st != 0:
-            raise binding.TgError(st, "tg_gemm_relu_f16")
+    if args.epilogue == "relu":
+        def step():
+            st = lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
+                                      wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU, handle)
+            if st != 0:
+                raise binding.TgError(st, "tg_gemm_relu_f16")
+    else:
+        from fp16_gemm_relu_gb300 import inputs as _inputs
+
+        bias = torch.from_numpy(_inputs.tensor(1, wl.N, wl.seed + 100, 0).ravel()).to(dev)
+        resid = None
+        act = binding.TG_ACT_GELU
+        if args.epilogue == "bias_relu_residual":
+            resid = torch.from_numpy(_inputs.tensor(wl.M, wl.N, wl.seed + 101, 1)).to(dev)
+            act = binding.TG_ACT_RELU
+        epi = binding.tg_epilogue(act, bias.data_ptr(), resid.data_ptr() if resid is not None else None,
+                                  wl.N if resid is not None else 0)
+
+        def step():
+            st = lib.tg_gemm_f16_epilogue(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N,
+                                          wl.K, wl.K, wl.N, wl.N, ctypes.byref(epi), None, handle)
+            if st != 0:
+                raise binding.TgError(st, "tg_gemm_f16_epilogue")
 
     bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
     sampler = ClockSampler(bus)
@@ -355,7 +376,7 @@ def run_ours(args, wl):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic (seeded SplitMix64 inputs of the workload's distribution)",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
-                   "accumulate": "f32", "output": "f16", "epilogue": "relu",
+                   "accumulate": "f32", "output": "f16", "epilogue": args.epilogue,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between steps" if flush else
                          f"inputs ({in_bytes / 2**20:.0f} MiB) larger than L2",

@@ -33,6 +33,14 @@ class tg_options(ctypes.Structure):
         "debug_flags", "timeout_ms", "pair")]
 
 
+class tg_epilogue(ctypes.Structure):
+    _fields_ = [("activation", ctypes.c_int), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p), ("ldr", ctypes.c_int64)]
+
+
+TG_ACT_NONE, TG_ACT_RELU, TG_ACT_GELU, TG_ACT_GELU_TANH = 0, 1, 2, 3
+
+
 class tg_plan(ctypes.Structure):
     _fields_ = [
         ("block_m", ctypes.c_int), ("block_n", ctypes.c_int), ("block_k", ctypes.c_int),
@@ -83,6 +91,8 @@ def load_library() -> ctypes.CDLL:
         L.tg_gemm_relu_f16_ex.argtypes = gemm_args + [ctypes.POINTER(tg_options), vp]
         L.tg_gemm_relu_f16_host.argtypes = gemm_args + [vp]
         L.tg_gemm_relu_f16_splitk_noalloc.argtypes = gemm_args + [ci, vp]
+        L.tg_gemm_f16_epilogue.argtypes = gemm_args[:9] + [ctypes.POINTER(tg_epilogue),
+                                                           ctypes.POINTER(tg_options), vp]
         L.tg_plan_query.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, ci,
                                     ctypes.POINTER(tg_options), ctypes.POINTER(tg_plan)]
         L.tg_device_error_check.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
@@ -92,7 +102,7 @@ def load_library() -> ctypes.CDLL:
         L.tg_release_workspace.argtypes = []
         L.tg_version.argtypes = []
         for name in ("tg_gemm_relu_f16", "tg_gemm_relu_f16_ex", "tg_gemm_relu_f16_host",
-                     "tg_gemm_relu_f16_splitk_noalloc",
+                     "tg_gemm_relu_f16_splitk_noalloc", "tg_gemm_f16_epilogue",
                      "tg_plan_query", "tg_device_error_check", "tg_last_cuda_error",
                      "tg_release_workspace", "tg_version"):
             getattr(L, name).restype = ci
@@ -125,6 +135,15 @@ def tg_gemm_relu_f16_ex(A: int, B: int, C: int, M: int, N: int, K: int, lda: int
                         ldc: int, epilogue_flag: int, options=None, stream: int = 0) -> int:
     return load_library().tg_gemm_relu_f16_ex(A, B, C, M, N, K, lda, ldb, ldc, epilogue_flag,
                                               _opts(options), stream or None)
+
+
+def tg_gemm_f16_epilogue(A: int, B: int, C: int, M: int, N: int, K: int, lda: int, ldb: int,
+                         ldc: int, activation: int = TG_ACT_NONE, bias: int = 0,
+                         residual: int = 0, ldr: int = 0, options=None, stream: int = 0) -> int:
+    """C = fp16(act(A·B + bias) + residual); bias/residual are device pointers or 0."""
+    e = tg_epilogue(activation, bias or None, residual or None, ldr)
+    return load_library().tg_gemm_f16_epilogue(A, B, C, M, N, K, lda, ldb, ldc,
+                                               ctypes.byref(e), _opts(options), stream or None)
 
 
 def tg_gemm_relu_f16_host(hA: int, hB: int, hC: int, M: int, N: int, K: int, lda: int,

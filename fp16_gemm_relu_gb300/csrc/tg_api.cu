@@ -304,12 +304,14 @@ __global__ void tg_pack_rows_kernel(const uint16_t* __restrict__ src, int64_t ld
   }
 }
 
-// C[i, j] = fp16(epi(sum_{s=0}^{splits-1} W[s][i][j])), the splits added in increasing s
-// (deterministic).  W rows are ldw floats (multiple of 4, 16-byte aligned); C may have any
-// 2-byte alignment and leading dimension.
+// C[i, j] = fp16(epilogue(sum_{s=0}^{splits-1} W[s][i][j])), the splits added in increasing s
+// (deterministic), then the same fused epilogue as the GEMM kernel (bias, activation,
+// residual).  W rows are ldw floats (multiple of 4, 16-byte aligned); C may have any 2-byte
+// alignment and leading dimension.  p supplies act, bias, residual, ldr, M and N.
 __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ldw,
-                                        int64_t split_stride, int splits, __half* __restrict__ C,
-                                        int64_t ldc, int64_t M, int64_t N, int relu) {
+                                        int64_t split_stride, int splits, __half* C,
+                                        int64_t ldc, const tg::GemmParams p) {
+  const int64_t M = p.M, N = p.N;
   const int64_t cpr = (N + 3) >> 2;
   const int64_t total = M * cpr;
   for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
@@ -317,7 +319,8 @@ __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ld
     const int64_t r = idx / cpr;
     const int64_t c0 = (idx - r * cpr) << 2;
     const float* w = ws + r * ldw + c0;
-    float4 acc = __ldg(reinterpret_cast<const float4*>(w));
+    // splits == 0: the empty sum (K == 0 with a bias or residual epilogue)
+    float4 acc = splits > 0 ? __ldg(reinterpret_cast<const float4*>(w)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 1; s < splits; ++s) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(w + s * split_stride));
       acc.x += v.x;
@@ -325,14 +328,11 @@ __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ld
       acc.z += v.z;
       acc.w += v.w;
     }
-    if (relu) {
-      acc.x = acc.x > 0.0f ? acc.x : 0.0f;
-      acc.y = acc.y > 0.0f ? acc.y : 0.0f;
-      acc.z = acc.z > 0.0f ? acc.z : 0.0f;
-      acc.w = acc.w > 0.0f ? acc.w : 0.0f;
-    }
-    __half h[4] = {__float2half_rn(acc.x), __float2half_rn(acc.y), __float2half_rn(acc.z),
-                   __float2half_rn(acc.w)};
+    float a[4] = {acc.x, acc.y, acc.z, acc.w};
+    __half h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      h[e] = __float2half_rn(c0 + e < N ? tg::epilogue_value(a[e], int(r), int(c0 + e), p) : 0.0f);
     __half* d = C + r * ldc + c0;
     if (c0 + 4 <= N && (reinterpret_cast<uintptr_t>(d) & 7u) == 0) {
       uint2 v;
@@ -373,17 +373,51 @@ CUresult encode_ws_3d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, con
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+tg_epilogue epilogue_from_flag(int flag) {
+  tg_epilogue e;
+  std::memset(&e, 0, sizeof(e));
+  e.activation = flag;
+  return e;
+}
+
+tg_status validate_epilogue(const tg_epilogue& e, const void* C, int64_t N, int64_t ldc) {
+  if (e.activation < TG_ACT_NONE || e.activation > TG_ACT_GELU_TANH) return TG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(e.bias) | reinterpret_cast<uintptr_t>(e.residual)) & 1u)
+    return TG_ERR_MISALIGNED;
+  if (e.residual) {
+    if (e.ldr < std::max<int64_t>(1, N) || e.ldr > (int64_t{1} << 36)) return TG_ERR_INVALID_ARG;
+    if (e.residual == C && e.ldr != ldc) return TG_ERR_INVALID_ARG;
+  }
+  return TG_OK;
+}
+
 tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                   int64_t lda, int64_t ldb, int64_t ldc, int flag, const tg_options* opt,
-                   cudaStream_t stream) {
-  tg_status st = validate(A, B, C, M, N, K, lda, ldb, ldc, flag);
+                   int64_t lda, int64_t ldb, int64_t ldc, const tg_epilogue& epi,
+                   const tg_options* opt, cudaStream_t stream) {
+  tg_status st = validate(A, B, C, M, N, K, lda, ldb, ldc, TG_EPILOGUE_NONE);
   if (st != TG_OK) return st;
+  if ((st = validate_epilogue(epi, C, N, ldc)) != TG_OK) return st;
   if (M == 0 || N == 0) return TG_OK;
   DeviceState* ds = nullptr;
   if ((st = current_device(&ds)) != TG_OK) return st;
   cudaError_t e;
-  if (K == 0) {
+  if (K == 0 && epi.bias == nullptr && epi.residual == nullptr) {
+    // act(+0) is +0 for every activation: the empty sum writes +0
     e = cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), stream);
+    return e == cudaSuccess ? TG_OK : cuda_fail(e);
+  }
+  if (K == 0) {  // C = act(0 + bias) + residual: the reduction pass over zero splits
+    tg::GemmParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    gp.act = epi.activation;
+    gp.bias = static_cast<const __half*>(epi.bias);
+    gp.residual = static_cast<const __half*>(epi.residual);
+    gp.ldr = epi.residual ? epi.ldr : 0;
+    gp.M = static_cast<int>(M);
+    gp.N = static_cast<int>(N);
+    tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
+        nullptr, 0, 0, 0, static_cast<__half*>(C), ldc, gp);
+    e = cudaGetLastError();
     return e == cudaSuccess ? TG_OK : cuda_fail(e);
   }
   Plan pl;
@@ -459,7 +493,10 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   gp.splits = P.split_k;
   gp.units = static_cast<int>(P.units);
   gp.panel_m = P.panel_m;
-  gp.relu = flag == TG_EPILOGUE_RELU ? 1 : 0;
+  gp.act = epi.activation;
+  gp.bias = static_cast<const __half*>(epi.bias);
+  gp.residual = static_cast<const __half*>(epi.residual);
+  gp.ldr = epi.residual ? epi.ldr : 0;
   gp.debug_flags = o.debug_flags;
   gp.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : kDefaultTimeoutMs);
   gp.err = ds->err;
@@ -481,7 +518,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
   if (ws) {
     tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
-        ws, pl.ldw, int64_t(M) * pl.ldw, P.split_k, static_cast<__half*>(C), ldc, M, N, gp.relu);
+        ws, pl.ldw, int64_t(M) * pl.ldw, P.split_k, static_cast<__half*>(C), ldc, gp);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
   }
   if (scratch && (e = cudaFreeAsync(scratch, stream)) != cudaSuccess) return cuda_fail(e);
@@ -499,10 +536,10 @@ cudaError_t error_word_address(unsigned int** out) {
 bool tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) { return encode_fn(fn) == TG_OK; }
 
 cudaError_t launch_splitk_reduce(const float* ws, int64_t ldw, int64_t split_stride, int splits,
-                                 void* C, int64_t ldc, int64_t M, int64_t N, int relu,
-                                 int num_sms, cudaStream_t stream) {
-  tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), num_sms), 256, 0, stream>>>(
-      ws, ldw, split_stride, splits, static_cast<__half*>(C), ldc, M, N, relu);
+                                 void* C, int64_t ldc, const GemmParams& p, int num_sms,
+                                 cudaStream_t stream) {
+  tg_splitk_reduce_kernel<<<aux_grid(int64_t(p.M) * cdiv(p.N, 4), num_sms), 256, 0, stream>>>(
+      ws, ldw, split_stride, splits, static_cast<__half*>(C), ldc, p);
   return cudaGetLastError();
 }
 
@@ -528,14 +565,27 @@ extern "C" {
 tg_status tg_gemm_relu_f16(const void* A, const void* B, void* C, int64_t M, int64_t N,
                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int epilogue_flag,
                            tg_stream_t stream) {
-  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc, epilogue_flag, nullptr,
+  if (epilogue_flag != TG_EPILOGUE_NONE && epilogue_flag != TG_EPILOGUE_RELU)
+    return TG_ERR_INVALID_ARG;
+  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc, epilogue_from_flag(epilogue_flag), nullptr,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
 tg_status tg_gemm_relu_f16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
                               int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                               int epilogue_flag, const tg_options* opt, tg_stream_t stream) {
-  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc, epilogue_flag, opt,
+  if (epilogue_flag != TG_EPILOGUE_NONE && epilogue_flag != TG_EPILOGUE_RELU)
+    return TG_ERR_INVALID_ARG;
+  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc, epilogue_from_flag(epilogue_flag), opt,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tg_gemm_f16_epilogue(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                               int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                               const tg_epilogue* epi, const tg_options* opt,
+                               tg_stream_t stream) {
+  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc,
+                  epi ? *epi : epilogue_from_flag(TG_EPILOGUE_NONE), opt,
                   reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -587,7 +637,8 @@ tg_status tg_gemm_relu_f16_host(const void* hA, const void* hB, void* hC, int64_
       st = cuda_fail(e);
   }
   if (st == TG_OK)
-    st = run_gemm(dA, dB, dC, M, N, K, lda_d, ldb_d, ldc_d, epilogue_flag, nullptr, stream);
+    st = run_gemm(dA, dB, dC, M, N, K, lda_d, ldb_d, ldc_d, epilogue_from_flag(epilogue_flag),
+                  nullptr, stream);
   if (st == TG_OK &&
       (e = cudaMemcpy2DAsync(hC, size_t(ldc) * 2, dC, size_t(ldc_d) * 2, size_t(N) * 2,
                              size_t(M), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)

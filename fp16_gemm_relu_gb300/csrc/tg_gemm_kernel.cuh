@@ -52,7 +52,7 @@ struct GemmParams {
   int splits;
   int units;           // tiles_m * tiles_n * splits
   int panel_m;
-  int relu;
+  int act;             // epilogue activation: kActNone, kActRelu, kActGelu, kActGeluTanh
   int debug_flags;
   unsigned long long timeout_ns;
   unsigned int* err;
@@ -62,7 +62,38 @@ struct GemmParams {
   __half* c;
   long long ldc;
   int M, N, n_tma;
+  // optional fused epilogue operands (fp16 output only): bias[j] added to column j before the
+  // activation, residual[i*ldr + j] added after it
+  const __half* bias;
+  const __half* residual;
+  long long ldr;
 };
+
+enum : int { kActNone = 0, kActRelu = 1, kActGelu = 2, kActGeluTanh = 3 };
+
+// The activations of the fused epilogue, in float32:
+//   relu(x)      = x > 0 ? x : +0                      (-0 and NaN give +0)
+//   gelu(x)      = x/2 * (1 + erf(x / sqrt 2))          (Hendrycks & Gimpel, 2016)
+//   gelu_tanh(x) = x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))   (same paper)
+__device__ __forceinline__ float activation(float x, int act) {
+  switch (act) {
+    case kActRelu: return x > 0.0f ? x : 0.0f;
+    case kActGelu: return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+    case kActGeluTanh: {
+      const float u = 0.79788456080286536f * (x + 0.044715f * x * x * x);
+      return 0.5f * x * (1.0f + tanhf(u));
+    }
+    default: return x;
+  }
+}
+
+// Full epilogue of one float32 sum at (row, col): (sum + bias) -> activation -> + residual.
+__device__ __forceinline__ float epilogue_value(float x, int row, int col, const GemmParams& p) {
+  if (p.bias) x += __half2float(p.bias[col]);
+  x = activation(x, p.act);
+  if (p.residual) x += __half2float(p.residual[static_cast<long long>(row) * p.ldr + col]);
+  return x;
+}
 
 template <int BN>
 struct TileCfg {
@@ -458,13 +489,31 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
       tmem_ld_x32(tl + c * 64 + 32, r1);
       tmem_wait_ld(r1);
       if (c == BN / 64 - 1) release();
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.relu);
-        pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.relu);
-      }
       const int col0 = col_base + c * 64;
+      uint32_t pk[32];
+      if (p.bias == nullptr && p.residual == nullptr && p.act <= kActRelu) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.act);
+          pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.act);
+        }
+      } else {
+        // general fused epilogue; columns past N and rows past M are computed but never stored
+        const int row = row0 + lane;
+        const bool row_ok = row < p.M;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t* src = i < 16 ? r0 : r1;
+          const int j = 2 * (i & 15);
+          const int ca = col0 + 2 * i, cb = ca + 1;
+          float x = __uint_as_float(src[j]);
+          float y = __uint_as_float(src[j + 1]);
+          x = (ca < p.N && row_ok) ? epilogue_value(x, row, ca, p) : 0.0f;
+          y = (cb < p.N && row_ok) ? epilogue_value(y, row, cb, p) : 0.0f;
+          __half2 h = __floats2half2_rn(x, y);
+          pk[i] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      }
       if (col0 < p.n_tma) {
         uint8_t* st = stg + sb * kStagingBuf;
         if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done

@@ -38,8 +38,9 @@ cudaError_t error_word_address(unsigned int** out);
 bool tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn);
 
 // Deterministic split-K reduction: C = fp16(epi(sum_s W[s])) (see tg_splitk_reduce_kernel).
+// p supplies the epilogue (act, bias, residual, ldr) and the shape (M, N).
 cudaError_t launch_splitk_reduce(const float* ws, int64_t ldw, int64_t split_stride, int splits,
-                                 void* C, int64_t ldc, int64_t M, int64_t N, int relu,
-                                 int num_sms, cudaStream_t stream);
+                                 void* C, int64_t ldc, const GemmParams& p, int num_sms,
+                                 cudaStream_t stream);
 
 }  // namespace tg

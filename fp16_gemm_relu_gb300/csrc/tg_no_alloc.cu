@@ -152,15 +152,17 @@ extern "C" tg_status tg_gemm_relu_f16_splitk_noalloc(const void* A, const void* 
   p.splits = static_cast<int>(splits);
   p.units = static_cast<int>(units);
   p.panel_m = static_cast<int>(std::min<int64_t>(kPanel, tiles_m));
-  p.relu = epilogue_flag == TG_EPILOGUE_RELU ? 1 : 0;
+  p.act = epilogue_flag == TG_EPILOGUE_RELU ? tg::kActRelu : tg::kActNone;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
   p.debug_flags = 0;
   p.timeout_ns = kTimeoutNs;
   p.err = su->err;
   L.grid = static_cast<int>(std::min<int64_t>(units, su->sm_count));
   L.stream = stream;
   if (tg::launch_gemm_bn256(L, /*out_f32=*/true) != cudaSuccess) return TG_ERR_CUDA;
-  if (tg::launch_splitk_reduce(su->workspace, ldw, M * ldw, static_cast<int>(splits), C, ldc, M,
-                               N, p.relu, su->sm_count, stream) != cudaSuccess)
+  if (tg::launch_splitk_reduce(su->workspace, ldw, M * ldw, static_cast<int>(splits), C, ldc, p,
+                               su->sm_count, stream) != cudaSuccess)
     return TG_ERR_CUDA;
   return TG_OK;
 }

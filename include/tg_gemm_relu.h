@@ -51,6 +51,22 @@ typedef enum {
 
 enum { TG_EPILOGUE_NONE = 0, TG_EPILOGUE_RELU = 1 };
 
+/* Activations of the fused epilogue (tg_gemm_f16_epilogue).  The first two equal the
+ * TG_EPILOGUE_* flags.  GELU is x/2 * (1 + erf(x/sqrt 2)); GELU_TANH is the tanh form
+ * x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))) (Hendrycks & Gimpel, 2016). */
+enum { TG_ACT_NONE = 0, TG_ACT_RELU = 1, TG_ACT_GELU = 2, TG_ACT_GELU_TANH = 3 };
+
+/* Fused epilogue: C = fp16( act( A·B + bias ) + residual ), every step in float32 and one
+ * rounding to fp16 at the end. */
+typedef struct {
+  int activation;         /* TG_ACT_* */
+  const void* bias;       /* NULL, or device fp16[N]: bias[j] is added to column j */
+  const void* residual;   /* NULL, or device fp16 M x N (leading dimension ldr) added after the
+                             activation; it may be C itself (same pointer, ldr == ldc), and
+                             must not otherwise overlap C */
+  int64_t ldr;
+} tg_epilogue;
+
 /*
  * C = fp16(relu(A·B)) (epilogue_flag = TG_EPILOGUE_RELU) or C = fp16(A·B) (TG_EPILOGUE_NONE).
  * A, B, C: device pointers to fp16 data, owned by the caller.  Asynchronous on `stream`:
@@ -104,6 +120,18 @@ typedef struct {
 tg_status tg_gemm_relu_f16_ex(const void* A, const void* B, void* C, int64_t M, int64_t N,
                               int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                               int epilogue_flag, const tg_options* opt, tg_stream_t stream);
+
+/*
+ * GEMM with the fused bias / activation / residual epilogue.  The pages motivate fusing the
+ * epilogue into the GEMM (the practitioner page, section 2: fusion keeps intermediates on chip)
+ * and use relu as their example (TileLang paper-reading page, section 2).  epi == NULL is
+ * the identity epilogue.  Other arguments, layouts and errors as tg_gemm_relu_f16_ex; bias and
+ * residual need 2-byte alignment; ldr >= max(1, N) when residual is given.
+ */
+tg_status tg_gemm_f16_epilogue(const void* A, const void* B, void* C, int64_t M, int64_t N,
+                               int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                               const tg_epilogue* epi, const tg_options* opt,
+                               tg_stream_t stream);
 
 /*
  * The plan tg_gemm_relu_f16_ex would use for these arguments on a device with num_sms SMs.

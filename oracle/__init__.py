@@ -40,6 +40,9 @@ def lib() -> ctypes.CDLL:
                      "tg_oracle_f16_to_f64_array"):
             getattr(L, name).restype = None
             getattr(L, name).argtypes = [p, p, i64]
+        L.tg_oracle_gemm_epilogue.restype = ctypes.c_int
+        L.tg_oracle_gemm_epilogue.argtypes = [p, p, i64, i64, i64, i64, i64, p, i64, p, i64,
+                                              ctypes.c_int, p, p, i64, p, p, p, ctypes.c_int]
         L.tg_oracle_max_threads.restype = ctypes.c_int
         L.tg_oracle_max_threads.argtypes = []
         _lib = L
@@ -119,6 +122,43 @@ def gemm_relu(A, B, relu: bool = True, rows=None, cols=None, lda=None, ldb=None,
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return res
+
+
+ACT = {"none": 0, "relu": 1, "gelu": 2, "gelu_tanh": 3}
+
+
+def gemm_epilogue(A, B, act="none", bias=None, residual=None, rows=None, cols=None,
+                  threads: int = 0) -> dict:
+    """fp16(act(A·B + bias) + residual) on the rows x cols sub-grid (all of C by default).
+
+    A (M,K), B (K,N) fp16; bias fp16[N] or None; residual fp16 (M, N) or None.  Returns
+    ``out16_f32acc`` and ``out16_f64acc`` (fp16 bits) and ``pre_f64`` (float64 sum + bias,
+    before the activation)."""
+    A = np.ascontiguousarray(A)
+    B = np.ascontiguousarray(B)
+    M, K = A.shape
+    N = B.shape[1]
+    a = ACT[act] if isinstance(act, str) else int(act)
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, np.int64)
+    cols = np.arange(N, dtype=np.int64) if cols is None else np.ascontiguousarray(cols, np.int64)
+    nr, nc = rows.size, cols.size
+    o32 = np.empty((nr, nc), np.uint16)
+    o64 = np.empty((nr, nc), np.uint16)
+    pre = np.empty((nr, nc), np.float64)
+    nullp = ctypes.c_void_p(None)
+    bb = None if bias is None else np.ascontiguousarray(bias, dtype=np.float16).view(np.uint16)
+    rr = None if residual is None else np.ascontiguousarray(residual, dtype=np.float16).view(np.uint16)
+    if bb is not None and bb.size != N:
+        raise ValueError("bias must have N elements")
+    ldr = 0 if rr is None else rr.shape[1]
+    rc = lib().tg_oracle_gemm_epilogue(
+        _ptr(A.view(np.uint16)), _ptr(B.view(np.uint16)), M, N, K, max(K, 1), max(N, 1),
+        _ptr(rows) if nr else nullp, nr, _ptr(cols) if nc else nullp, nc, a,
+        _ptr(bb) if bb is not None else nullp, _ptr(rr) if rr is not None else nullp, ldr,
+        _ptr(o32), _ptr(o64), _ptr(pre), int(threads))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return {"out16_f32acc": o32, "out16_f64acc": o64, "pre_f64": pre}
 
 
 def timed_rows(A, B, nrows: int, relu: bool = True, threads: int = 0):

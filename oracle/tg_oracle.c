@@ -172,3 +172,66 @@ int tg_oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* ---- fused epilogue: C = fp16( act( sum + bias[j] ) + residual[i, j] ) ----
+ *
+ * The pages motivate fusing the elementwise epilogue into the GEMM (the practitioner page,
+ * section 2) and use relu as the example (the paper-reading page, section 2).  Activations:
+ *   relu(x)      = x > 0 ? x : +0
+ *   gelu(x)      = x/2 * (1 + erf(x / sqrt 2))
+ *   gelu_tanh(x) = x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))
+ * (GELU and its tanh form: Hendrycks & Gimpel, "Gaussian Error Linear Units", 2016.)
+ * The float64 result adds bias, applies the activation with libm's erf/tanh and adds the
+ * residual in double, then rounds once to fp16; the float32 result does the same steps in
+ * float (activation evaluated in double and rounded to float).
+ */
+static double act64(double x, int act) {
+  switch (act) {
+    case 1: return (x > 0.0) ? x : 0.0;
+    case 2: return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+    case 3: return 0.5 * x * (1.0 + tanh(sqrt(2.0 / acos(-1.0)) * (x + 0.044715 * x * x * x)));
+    default: return x;
+  }
+}
+
+int tg_oracle_gemm_epilogue(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, const int64_t* rows, int64_t nr,
+                            const int64_t* cols, int64_t nc, int act, const uint16_t* bias,
+                            const uint16_t* residual, int64_t ldr, uint16_t* out16_f32acc,
+                            uint16_t* out16_f64acc, double* pre_f64, int nthreads) {
+  if (act < 0 || act > 3) return -1;
+  if (residual && ldr < N) return -1;
+  if (nr == 0 || nc == 0) return 0;
+  float* s32 = (float*)malloc(sizeof(float) * (size_t)nr * (size_t)nc);
+  double* s64 = (double*)malloc(sizeof(double) * (size_t)nr * (size_t)nc);
+  if (!s32 || !s64) {
+    free(s32);
+    free(s64);
+    return -1;
+  }
+  int rc = tg_oracle_gemm_relu(A, B, M, N, K, lda, ldb, rows, nr, cols, nc, 0, NULL, s32, NULL,
+                               s64, nthreads);
+  if (rc == 0) {
+    for (int64_t r = 0; r < nr; ++r) {
+      for (int64_t c = 0; c < nc; ++c) {
+        const int64_t o = r * nc + c;
+        const int64_t i = rows[r], j = cols[c];
+        double b = bias ? tg_oracle_f16_to_f64(bias[j]) : 0.0;
+        double res = residual ? tg_oracle_f16_to_f64(residual[i * ldr + j]) : 0.0;
+        /* float64 reference */
+        double x = s64[o] + b;
+        if (pre_f64) pre_f64[o] = x;
+        double y = act64(x, act) + res;
+        if (out16_f64acc) out16_f64acc[o] = tg_oracle_f64_to_f16(y);
+        /* float32 steps */
+        float xf = s32[o] + (float)b;
+        float yf = (float)act64((double)xf, act);
+        yf = yf + (float)res;
+        if (out16_f32acc) out16_f32acc[o] = tg_oracle_f32_to_f16(yf);
+      }
+    }
+  }
+  free(s32);
+  free(s64);
+  return rc;
+}

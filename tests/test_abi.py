@@ -132,3 +132,14 @@ def test_plan_overrides(lib):
 def test_plan_k_zero_and_empty(lib):
     assert _plan(10, 10, 0)["kernels"] == 1
     assert _plan(0, 10, 10)["kernels"] == 0
+
+
+def test_epilogue_argument_errors(lib):
+    # rejected by host validation before any device work
+    p = 4096
+    e = binding.tg_gemm_f16_epilogue
+    assert e(p, p, p, 4, 4, 4, 4, 4, 4, 9) == binding.TG_ERR_INVALID_ARG        # activation
+    assert e(p, p, p, 4, 4, 4, 4, 4, 4, 1, p + 1) == binding.TG_ERR_MISALIGNED  # bias
+    assert e(p, p, p, 4, 4, 4, 4, 4, 4, 1, 0, p, 3) == binding.TG_ERR_INVALID_ARG  # ldr < N
+    assert e(p, p, p, 4, 4, 4, 4, 4, 8, 1, 0, p, 4) == binding.TG_ERR_INVALID_ARG  # C alias, ldr != ldc
+    assert e(0, 0, 0, 0, 4, 4, 4, 4, 4, 2) == binding.TG_OK                       # empty
