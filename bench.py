@@ -43,6 +43,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="square8192", choices=workloads.ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
+                    help="backward: one step = dZ = relu'(C) * dC, dA = dZ B^T, dB = A^T dZ "
+                         "(4MNK flops), all in the library's kernels")
     ap.add_argument("--epilogue", default="relu", choices=["relu", "bias_gelu", "bias_relu_residual"],
                     help="relu: the metric's path; the others time the fused bias/GELU/residual "
                          "epilogue on the same GEMM")
@@ -278,7 +281,34 @@ def run_ours(args, wl):
     handle = stream.cuda_stream
     lib = binding.load_library()
 
-    if args.epilogue == "relu":
+    flops_per_step = wl.flops
+    if args.pass_ == "backward":
+        # gradients of C = relu(A·B) for a seeded dC; the step is mask + two GEMMs
+        from fp16_gemm_relu_gb300 import inputs as _inputs
+
+        st = lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
+                                  wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU, handle)
+        if st != 0:
+            raise binding.TgError(st, "tg_gemm_relu_f16")
+        dC = torch.from_numpy(_inputs.tensor(wl.M, wl.N, wl.seed + 102, 1)).to(dev)
+        dZ = torch.empty_like(dC)
+        dA = torch.empty_like(A)
+        dB = torch.empty_like(B)
+        flops_per_step = 2 * wl.flops
+        plan = {**plan, "kernels": 3}
+
+        def step():
+            st = lib.tg_relu_backward_f16(dC.data_ptr(), C.data_ptr(), dZ.data_ptr(), wl.M, wl.N,
+                                          wl.N, wl.N, wl.N, handle)
+            if st == 0:
+                st = lib.tg_gemm_f16_t(0, 1, dZ.data_ptr(), B.data_ptr(), dA.data_ptr(), wl.M,
+                                       wl.K, wl.N, wl.N, wl.N, wl.K, None, None, handle)
+            if st == 0:
+                st = lib.tg_gemm_f16_t(1, 0, A.data_ptr(), dZ.data_ptr(), dB.data_ptr(), wl.K,
+                                       wl.N, wl.M, wl.K, wl.N, wl.N, None, None, handle)
+            if st != 0:
+                raise binding.TgError(st, "backward step")
+    elif args.epilogue == "relu":
         def step():
             st = lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
                                       wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU, handle)
@@ -339,7 +369,7 @@ def run_ours(args, wl):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = world * args.steps * wl.flops / (total_ms * 1e-3) / 1e12
+    value = world * args.steps * flops_per_step / (total_ms * 1e-3) / 1e12
     st, word = binding.tg_device_error_check(clear=True)
     if st != 0:
         raise RuntimeError(f"device error word {word:#x} after the timed region")
@@ -351,7 +381,7 @@ def run_ours(args, wl):
     t_tensor = wl.flops / (peaks["bf16_tflops"] * FP16_OVER_BF16 * 1e12)
     t_hbm = wl.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
     if t_tensor >= t_hbm:
-        achieved = wl.flops / (kernel_ms * 1e-3) / 1e12
+        achieved = flops_per_step / (kernel_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"] * FP16_OVER_BF16, "unit": "TFLOP/s"}
     else:
@@ -377,6 +407,7 @@ def run_ours(args, wl):
         "data": "synthetic (seeded SplitMix64 inputs of the workload's distribution)",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                    "accumulate": "f32", "output": "f16", "epilogue": args.epilogue,
+                   "pass": args.pass_,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between steps" if flush else
                          f"inputs ({in_bytes / 2**20:.0f} MiB) larger than L2",
@@ -387,7 +418,7 @@ def run_ours(args, wl):
         "clocks": sampler.summary(),
     }
 
-    if rank == 0 and not args.no_e2e:
+    if rank == 0 and not args.no_e2e and args.pass_ == "forward":
         line["e2e"] = e2e(wl, A_h, B_h, dev, max(3, min(args.steps, 10)))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, a_np, b_np, args.cpu_seconds)

@@ -93,6 +93,9 @@ def load_library() -> ctypes.CDLL:
         L.tg_gemm_relu_f16_splitk_noalloc.argtypes = gemm_args + [ci, vp]
         L.tg_gemm_f16_epilogue.argtypes = gemm_args[:9] + [ctypes.POINTER(tg_epilogue),
                                                            ctypes.POINTER(tg_options), vp]
+        L.tg_gemm_f16_t.argtypes = [ci, ci] + gemm_args[:9] + [ctypes.POINTER(tg_epilogue),
+                                                              ctypes.POINTER(tg_options), vp]
+        L.tg_relu_backward_f16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, vp]
         L.tg_plan_query.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, ci,
                                     ctypes.POINTER(tg_options), ctypes.POINTER(tg_plan)]
         L.tg_device_error_check.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
@@ -103,6 +106,7 @@ def load_library() -> ctypes.CDLL:
         L.tg_version.argtypes = []
         for name in ("tg_gemm_relu_f16", "tg_gemm_relu_f16_ex", "tg_gemm_relu_f16_host",
                      "tg_gemm_relu_f16_splitk_noalloc", "tg_gemm_f16_epilogue",
+                     "tg_gemm_f16_t", "tg_relu_backward_f16",
                      "tg_plan_query", "tg_device_error_check", "tg_last_cuda_error",
                      "tg_release_workspace", "tg_version"):
             getattr(L, name).restype = ci
@@ -144,6 +148,20 @@ def tg_gemm_f16_epilogue(A: int, B: int, C: int, M: int, N: int, K: int, lda: in
     e = tg_epilogue(activation, bias or None, residual or None, ldr)
     return load_library().tg_gemm_f16_epilogue(A, B, C, M, N, K, lda, ldb, ldc,
                                                ctypes.byref(e), _opts(options), stream or None)
+
+
+def tg_gemm_f16_t(trans_a: int, trans_b: int, A: int, B: int, C: int, M: int, N: int, K: int,
+                  lda: int, ldb: int, ldc: int, activation: int = TG_ACT_NONE, bias: int = 0,
+                  residual: int = 0, ldr: int = 0, options=None, stream: int = 0) -> int:
+    """C = fp16(act(op(A)·op(B) + bias) + residual), op = transpose when trans_* is 1."""
+    e = tg_epilogue(activation, bias or None, residual or None, ldr)
+    return load_library().tg_gemm_f16_t(trans_a, trans_b, A, B, C, M, N, K, lda, ldb, ldc,
+                                        ctypes.byref(e), _opts(options), stream or None)
+
+
+def tg_relu_backward_f16(dC: int, C: int, dZ: int, M: int, N: int, lddc: int, ldc: int,
+                         lddz: int, stream: int = 0) -> int:
+    return load_library().tg_relu_backward_f16(dC, C, dZ, M, N, lddc, ldc, lddz, stream or None)
 
 
 def tg_gemm_relu_f16_host(hA: int, hB: int, hC: int, M: int, N: int, K: int, lda: int,

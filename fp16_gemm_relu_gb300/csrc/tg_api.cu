@@ -107,12 +107,14 @@ tg_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
 
+// ta / tb: A stored K x M (row length M) / B stored N x K (row length K) instead of M x K / K x N.
 tg_status validate(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                   int64_t lda, int64_t ldb, int64_t ldc, int flag) {
+                   int64_t lda, int64_t ldb, int64_t ldc, int flag, int ta = 0, int tb = 0) {
   if (M < 0 || N < 0 || K < 0) return TG_ERR_INVALID_ARG;
   if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return TG_ERR_INVALID_ARG;
   if (flag != TG_EPILOGUE_NONE && flag != TG_EPILOGUE_RELU) return TG_ERR_INVALID_ARG;
-  if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) ||
+  if ((ta != 0 && ta != 1) || (tb != 0 && tb != 1)) return TG_ERR_INVALID_ARG;
+  if (lda < std::max<int64_t>(1, ta ? M : K) || ldb < std::max<int64_t>(1, tb ? K : N) ||
       ldc < std::max<int64_t>(1, N))
     return TG_ERR_INVALID_ARG;
   if (lda > (int64_t{1} << 36) || ldb > (int64_t{1} << 36) || ldc > (int64_t{1} << 36))
@@ -148,7 +150,7 @@ double kblock_cycles(int bn) {
 // 60% of the SMs busy; plus the float32 workspace traffic of split-K and its extra launch.
 tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N, int64_t K,
                     int64_t lda, int64_t ldb, int64_t ldc, int num_sms, int pair_clusters,
-                    const tg_options* opt, Plan* out) {
+                    const tg_options* opt, Plan* out, int ta = 0, int tb = 0) {
   tg_options o;
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
@@ -256,15 +258,15 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   P.workspace_epilogue = (P.split_k > 1 || !c_direct) ? 1 : 0;
 
   int64_t off = 0;
-  if (P.repack_a) {
-    pl.lda_p = round_up(K, 8);
+  if (P.repack_a) {  // A is stored (ta ? K x M : M x K)
+    pl.lda_p = round_up(ta ? M : K, 8);
     pl.off_a = off;
-    off += round_up(M * pl.lda_p * 2, 256);
+    off += round_up((ta ? K : M) * pl.lda_p * 2, 256);
   }
-  if (P.repack_b) {
-    pl.ldb_p = round_up(N, 8);
+  if (P.repack_b) {  // B is stored (tb ? N x K : K x N)
+    pl.ldb_p = round_up(tb ? K : N, 8);
     pl.off_b = off;
-    off += round_up(K * pl.ldb_p * 2, 256);
+    off += round_up((tb ? N : K) * pl.ldb_p * 2, 256);
   }
   if (P.workspace_epilogue) {
     pl.ldw = round_up(N, 4);
@@ -345,6 +347,23 @@ __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ld
   }
 }
 
+// dZ[i, j] = C[i, j] > 0 ? dC[i, j] : +0 (the relu derivative taken on the forward output C;
+// NaN or -0 in C gives +0).  Any 2-byte alignment; one element per thread per step.
+__global__ void tg_relu_backward_kernel(const uint16_t* __restrict__ dC, int64_t lddc,
+                                        const uint16_t* __restrict__ C, int64_t ldc,
+                                        uint16_t* __restrict__ dZ, int64_t lddz, int64_t M,
+                                        int64_t N) {
+  const int64_t total = M * N;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = idx / N;
+    const int64_t c = idx - r * N;
+    const uint16_t cv = __ldg(C + r * ldc + c);
+    const bool pos = (cv & 0x8000u) == 0 && cv != 0 && (cv & 0x7FFFu) <= 0x7C00u;
+    dZ[r * lddz + c] = pos ? __ldg(dC + r * lddc + c) : uint16_t(0);
+  }
+}
+
 int aux_grid(int64_t work_items, int num_sms) {
   const int64_t blocks = cdiv(std::max<int64_t>(work_items, 1), 256);
   return static_cast<int>(std::min<int64_t>(blocks, int64_t(num_sms) * 8));
@@ -393,8 +412,8 @@ tg_status validate_epilogue(const tg_epilogue& e, const void* C, int64_t N, int6
 
 tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
                    int64_t lda, int64_t ldb, int64_t ldc, const tg_epilogue& epi,
-                   const tg_options* opt, cudaStream_t stream) {
-  tg_status st = validate(A, B, C, M, N, K, lda, ldb, ldc, TG_EPILOGUE_NONE);
+                   const tg_options* opt, cudaStream_t stream, int ta = 0, int tb = 0) {
+  tg_status st = validate(A, B, C, M, N, K, lda, ldb, ldc, TG_EPILOGUE_NONE, ta, tb);
   if (st != TG_OK) return st;
   if ((st = validate_epilogue(epi, C, N, ldc)) != TG_OK) return st;
   if (M == 0 || N == 0) return TG_OK;
@@ -423,7 +442,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   Plan pl;
   st = make_plan(reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
                  reinterpret_cast<uintptr_t>(C), M, N, K, lda, ldb, ldc, ds->sm_count,
-                 ds->pair_clusters, opt, &pl);
+                 ds->pair_clusters, opt, &pl, ta, tb);
   if (st != TG_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if ((st = encode_fn(&enc)) != TG_OK) return st;
@@ -449,7 +468,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   if (P.repack_a) {
     uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pl.off_a);
     tg_pack_rows_kernel<<<aux_grid(M * cdiv(K, 8), ds->sm_count), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(A), lda, dst, pl.lda_p, M, K);
+        static_cast<const uint16_t*>(A), lda, dst, pl.lda_p, ta ? K : M, ta ? M : K);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
     Ae = dst;
     lda_e = pl.lda_p;
@@ -457,7 +476,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   if (P.repack_b) {
     uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pl.off_b);
     tg_pack_rows_kernel<<<aux_grid(K * cdiv(N, 8), ds->sm_count), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(B), ldb, dst, pl.ldb_p, K, N);
+        static_cast<const uint16_t*>(B), ldb, dst, pl.ldb_p, tb ? N : K, tb ? K : N);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
     Be = dst;
     ldb_e = pl.ldb_p;
@@ -465,11 +484,17 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
   tg::GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
-  CUresult cr = encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(K), uint64_t(M),
-                          uint64_t(lda_e) * 2, tg::kBK, tg::kBM);
+  // A: K-major box {64 K, 128 rows} or, stored K x M, two MN-major boxes {64 M, 64 K};
+  // B: MN-major boxes {64 N, 64 K} or, stored N x K, one K-major box {64 K, BN (or 128) rows}
+  CUresult cr = ta ? encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(M),
+                               uint64_t(K), uint64_t(lda_e) * 2, 64, tg::kBK)
+                   : encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(K),
+                               uint64_t(M), uint64_t(lda_e) * 2, tg::kBK, tg::kBM);
   if (cr == CUDA_SUCCESS)
-    cr = encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(N), uint64_t(K),
-                   uint64_t(ldb_e) * 2, 64, tg::kBK);
+    cr = tb ? encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(K), uint64_t(N),
+                        uint64_t(ldb_e) * 2, tg::kBK, P.cta_pair ? 128u : uint32_t(P.block_n))
+            : encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(N), uint64_t(K),
+                        uint64_t(ldb_e) * 2, 64, tg::kBK);
   float* ws = P.workspace_epilogue ? reinterpret_cast<float*>(scratch + pl.off_w) : nullptr;
   if (cr == CUDA_SUCCESS) {
     if (ws)
@@ -497,6 +522,8 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   gp.bias = static_cast<const __half*>(epi.bias);
   gp.residual = static_cast<const __half*>(epi.residual);
   gp.ldr = epi.residual ? epi.ldr : 0;
+  gp.a_mn = ta;
+  gp.b_k = tb;
   gp.debug_flags = o.debug_flags;
   gp.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : kDefaultTimeoutMs);
   gp.err = ds->err;
@@ -587,6 +614,37 @@ tg_status tg_gemm_f16_epilogue(const void* A, const void* B, void* C, int64_t M,
   return run_gemm(A, B, C, M, N, K, lda, ldb, ldc,
                   epi ? *epi : epilogue_from_flag(TG_EPILOGUE_NONE), opt,
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+tg_status tg_gemm_f16_t(int trans_a, int trans_b, const void* A, const void* B, void* C,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        const tg_epilogue* epi, const tg_options* opt, tg_stream_t stream) {
+  if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return TG_ERR_INVALID_ARG;
+  return run_gemm(A, B, C, M, N, K, lda, ldb, ldc,
+                  epi ? *epi : epilogue_from_flag(TG_EPILOGUE_NONE), opt,
+                  reinterpret_cast<cudaStream_t>(stream), trans_a, trans_b);
+}
+
+tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t M, int64_t N,
+                               int64_t lddc, int64_t ldc, int64_t lddz, tg_stream_t stream) {
+  if (M < 0 || N < 0) return TG_ERR_INVALID_ARG;
+  if (lddc < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N) ||
+      lddz < std::max<int64_t>(1, N))
+    return TG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return TG_OK;
+  if (!dC || !C || !dZ) return TG_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dC) | reinterpret_cast<uintptr_t>(C) |
+       reinterpret_cast<uintptr_t>(dZ)) & 1u)
+    return TG_ERR_MISALIGNED;
+  DeviceState* ds = nullptr;
+  tg_status st = current_device(&ds);
+  if (st != TG_OK) return st;
+  tg_relu_backward_kernel<<<aux_grid(M * N, ds->sm_count), 256, 0,
+                            reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint16_t*>(dC), lddc, static_cast<const uint16_t*>(C), ldc,
+      static_cast<uint16_t*>(dZ), lddz, M, N);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }
 
 tg_status tg_plan_query(const void* A, const void* B, const void* C, int64_t M, int64_t N,

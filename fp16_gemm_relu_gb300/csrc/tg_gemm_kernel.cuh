@@ -53,6 +53,8 @@ struct GemmParams {
   int units;           // tiles_m * tiles_n * splits
   int panel_m;
   int act;             // epilogue activation: kActNone, kActRelu, kActGelu, kActGeluTanh
+  int a_mn;            // 1: A is stored K x M (M contiguous): MN-major tiles, two 64-wide boxes
+  int b_k;             // 1: B is stored N x K (K contiguous): K-major tiles, one {64, rows} box
   int debug_flags;
   unsigned long long timeout_ns;
   unsigned int* err;
@@ -371,24 +373,33 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
-// A tile: 128 rows (M) x 64 K, K contiguous ("K-major"); row r at r*128 bytes, 16-byte chunks
-// XOR-swizzled by r%8.  Canonical K-major SW128: 8-row groups 1024 bytes apart (SBO); LBO is
-// unused for swizzled K-major layouts (encoded as 16 bytes).  The k-th 16-wide K slice
-// starts 32*k bytes into the rows.
-__device__ __forceinline__ uint64_t desc_a_kmajor(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
+// K-major tile (A stored M x K, or B stored N x K): 128 (or BN) rows x 64 K, K contiguous;
+// row r at r*128 bytes, 16-byte chunks XOR-swizzled by r%8.  Canonical K-major SW128: 8-row
+// groups 1024 bytes apart (SBO); LBO is unused for swizzled K-major layouts (encoded as 16
+// bytes).  The k-th 16-wide K slice starts 32*k bytes into the rows.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr) { return sw128_desc(saddr, 16, 1024); }
 
-// B tile: 64 K rows x BN, N contiguous ("MN-major"), stored as BN/64 boxes of 64(N) x 64(K),
-// each box 8 KB with K row r at r*128 bytes.  Canonical MN-major SW128: consecutive 64-wide
-// N chunks are LBO = 8 KB apart, consecutive groups of 8 K rows are SBO = 1024 bytes apart.
-// The k-th 16-deep K slice starts 16*128*k = 2048*k bytes in.
-__device__ __forceinline__ uint64_t desc_b_mnmajor(uint32_t saddr) { return sw128_desc(saddr, 8192, 1024); }
+// MN-major tile (B stored K x N, or A stored K x M): 64 K rows x 128 or BN columns, stored
+// as boxes of 64 (N or M) x 64 (K), each 8 KB with K row r at r*128 bytes.  Canonical MN-major
+// SW128: consecutive 64-wide chunks are LBO = 8 KB apart, consecutive groups of 8 K rows are
+// SBO = 1024 bytes apart.  The k-th 16-deep K slice starts 16*128*k = 2048*k bytes in.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t saddr) { return sw128_desc(saddr, 8192, 1024); }
 
 // Instruction descriptor for kind::f16: D f32 (bits 4-5 = 1), A f16 (7-9 = 0), B f16
-// (10-12 = 0), A K-major (bit 15 = 0), B MN-major (bit 16 = 1), N>>3 at 17-22, M>>4 at 24-28.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
-  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (1u << 16) |
-         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+// (10-12 = 0), A major at bit 15 and B major at bit 16 (0: K-major, 1: MN-major), N>>3 at
+// 17-22, M>>4 at 24-28.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, int a_mn = 0, int b_mn = 1) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
 }
+
+// Operand tile descriptor and its per-16-K advance (in 16-byte units) for either major:
+// K-major tiles advance 32 bytes along the 128-byte row, MN-major tiles advance 16 rows.
+__device__ __forceinline__ uint64_t desc_operand(uint32_t saddr, int mn_major) {
+  return mn_major ? desc_mnmajor(saddr) : desc_kmajor(saddr);
+}
+__device__ __forceinline__ uint64_t desc_k_step(int mn_major) { return mn_major ? 128u : 2u; }
 
 // ---------------------------------------------------------------------------------------
 // Work decomposition
@@ -460,6 +471,70 @@ __device__ __forceinline__ uint32_t relu_pack_h2(uint32_t a, uint32_t b, int rel
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Loads 32 fp16 values v[0..31] = src[col .. col+31] (zeros past n): four 16-byte loads when
+// the address is 16-byte aligned and all 32 are in range, else guarded 2-byte loads.
+__device__ __forceinline__ void load_half32(const __half* src, int col, int n, float (&v)[32]) {
+  const __half* q = src + col;
+  if (col + 32 <= n && (reinterpret_cast<uintptr_t>(q) & 15u) == 0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(q) + j);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[e]));
+        v[8 * j + 2 * e] = f.x;
+        v[8 * j + 2 * e + 1] = f.y;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = (col + i < n) ? __half2float(q[i]) : 0.0f;
+  }
+}
+
+// General fused epilogue of 32 consecutive columns of one row: x = acc + bias, activation,
+// + residual, then fp16 pairs into pk[0..15].
+__device__ __forceinline__ void epilogue_general_32(const uint32_t (&acc)[32], int row, int col,
+                                                    const GemmParams& p, uint32_t* pk) {
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(acc[i]);
+  if (p.bias) {
+    float b[32];
+    load_half32(p.bias, col, p.N, b);  // the same 64 bytes for every lane: broadcast
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] += b[i];
+  }
+  switch (p.act) {
+    case kActRelu:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = activation(x[i], kActRelu);
+      break;
+    case kActGelu:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = activation(x[i], kActGelu);
+      break;
+    case kActGeluTanh:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = activation(x[i], kActGeluTanh);
+      break;
+    default:
+      break;
+  }
+  if (p.residual && row < p.M) {
+    float r[32];
+    load_half32(p.residual + static_cast<long long>(row) * p.ldr, col, p.N, r);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] += r[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+    pk[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
 // One output tile's epilogue for one warp: TMEM lane quarter at `tl` (32 rows starting at
 // row0, BN columns starting at col_base) -> registers -> epilogue -> 128B-swizzled staging ->
 // TMA store.  After the last tcgen05.ld the warp releases the accumulator by arriving on
@@ -498,21 +573,10 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
           pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.act);
         }
       } else {
-        // general fused epilogue; columns past N and rows past M are computed but never stored
-        const int row = row0 + lane;
-        const bool row_ok = row < p.M;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t* src = i < 16 ? r0 : r1;
-          const int j = 2 * (i & 15);
-          const int ca = col0 + 2 * i, cb = ca + 1;
-          float x = __uint_as_float(src[j]);
-          float y = __uint_as_float(src[j + 1]);
-          x = (ca < p.N && row_ok) ? epilogue_value(x, row, ca, p) : 0.0f;
-          y = (cb < p.N && row_ok) ? epilogue_value(y, row, cb, p) : 0.0f;
-          __half2 h = __floats2half2_rn(x, y);
-          pk[i] = *reinterpret_cast<uint32_t*>(&h);
-        }
+        // general fused epilogue, 32 columns at a time; columns past N and rows past M are
+        // computed but never stored
+        epilogue_general_32(r0, row0 + lane, col0, p, pk);
+        epilogue_general_32(r1, row0 + lane, col0 + 32, p, pk + 16);
       }
       if (col0 < p.n_tma) {
         uint8_t* st = stg + sb * kStagingBuf;
@@ -573,8 +637,8 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
 // ---------------------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------------------
-// tmA:   fp16 A, dims {K, M}, box {64, 128}, 128B swizzle
-// tmB:   fp16 B, dims {N, K}, box {64, 64}, 128B swizzle
+// tmA:   fp16 A, dims {K, M}, box {64, 128}, 128B swizzle   (p.a_mn: dims {M, K}, box {64, 64})
+// tmB:   fp16 B, dims {N, K}, box {64, 64}, 128B swizzle    (p.b_k: dims {K, N}, box {64, BN})
 // tmOut: OUT_F32 == false: fp16 C, dims {n_tma, M}, box {64, 32}, 128B swizzle (columns
 //        [n_tma, N) are written with plain stores through p.c)
 //        OUT_F32 == true:  f32 workspace, dims {N, M, splits}, box {32, 32, 1}, 128B swizzle
@@ -648,11 +712,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             const uint32_t fb = smem_u32(&full[stage]);
             mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-            tma_load_2d(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, w.m_blk * kBM);
+            const uint32_t a_dst = smem_u32(sA + stage * Cfg::kAStage);
+            const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
+            if (!p.a_mn) {
+              tma_load_2d(a_dst, &tmA, fb, kb * kBK, w.m_blk * kBM);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j)
-              tma_load_2d(smem_u32(sB + stage * Cfg::kBStage + j * Cfg::kBBox), &tmB, fb,
-                          w.n_blk * BN + j * 64, kb * kBK);
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_2d(a_dst + j * 8192, &tmA, fb, w.m_blk * kBM + j * 64, kb * kBK);
+            }
+            if (!p.b_k) {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(b_dst + j * Cfg::kBBox, &tmB, fb, w.n_blk * BN + j * 64, kb * kBK);
+            } else {
+              tma_load_2d(b_dst, &tmB, fb, kb * kBK, w.n_blk * BN);
+            }
             armed |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -670,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(kBM, BN);
+      const uint32_t idesc = idesc_f16_f32(kBM, BN, p.a_mn, !p.b_k);
+      const uint64_t a_step = desc_k_step(p.a_mn), b_step = desc_k_step(!p.b_k);
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
@@ -688,14 +764,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_a_kmajor(smem_u32(sA + stage * Cfg::kAStage));
-          const uint64_t bd = desc_b_mnmajor(smem_u32(sB + stage * Cfg::kBStage));
+          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), p.a_mn);
+          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !p.b_k);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            // start-address field is in 16-byte units: A advances 32 B, B advances 2048 B
-            umma_f16(d_tmem, ad + static_cast<uint64_t>(2 * k), bd + static_cast<uint64_t>(128 * k),
-                     idesc, (kb > w.kb_begin || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
+                     (kb > w.kb_begin || k > 0) ? 1u : 0u);
           umma_commit(smem_u32(&empty[stage]));
           if (++stage == S) {
             stage = 0;
@@ -851,11 +925,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               armed |= 1u << stage;
               armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             }
-            tma_load_2d_pair(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, arow);
+            const uint32_t a_dst = smem_u32(sA + stage * Cfg::kAStage);
+            const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
+            if (!p.a_mn) {
+              tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, arow);
+            } else {
 #pragma unroll
-            for (int j = 0; j < Cfg::kHalfN / 64; ++j)
-              tma_load_2d_pair(smem_u32(sB + stage * Cfg::kBStage + j * Cfg::kBBox), &tmB, fb,
-                               bcol + j * 64, kb * kBK);
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_2d_pair(a_dst + j * 8192, &tmA, fb, arow + j * 64, kb * kBK);
+            }
+            if (!p.b_k) {
+#pragma unroll
+              for (int j = 0; j < Cfg::kHalfN / 64; ++j)
+                tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
+            } else {
+              tma_load_2d_pair(b_dst, &tmB, fb, kb * kBK, bcol);
+            }
           }
           if (++stage == S) {
             stage = 0;
@@ -872,7 +957,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer (leader) ------------------------------
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN);
+      const uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN, p.a_mn, !p.b_k);
+      const uint64_t a_step = desc_k_step(p.a_mn), b_step = desc_k_step(!p.b_k);
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
@@ -890,12 +976,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_a_kmajor(smem_u32(sA + stage * Cfg::kAStage));
-          const uint64_t bd = desc_b_mnmajor(smem_u32(sB + stage * Cfg::kBStage));
+          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), p.a_mn);
+          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !p.b_k);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_f16_pair(d_tmem, ad + static_cast<uint64_t>(2 * k),
-                          bd + static_cast<uint64_t>(128 * k), idesc,
+            umma_f16_pair(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
                           (kb > w.kb_begin || k > 0) ? 1u : 0u);
           umma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
           if (++stage == S) {

@@ -134,6 +134,27 @@ tg_status tg_gemm_f16_epilogue(const void* A, const void* B, void* C, int64_t M,
                                tg_stream_t stream);
 
 /*
+ * C = fp16(epilogue(op(A)·op(B))) with op(A) M x K and op(B) K x N, for the backward pass of
+ * relu(A·B) (the practitioner page, section 3.3: the kernel behind torch.autograd.Function
+ * needs its own backward kernels).
+ *   trans_a = 0: A stored M x K row-major (lda >= K);  1: A stored K x M row-major (lda >= M)
+ *   trans_b = 0: B stored K x N row-major (ldb >= N);  1: B stored N x K row-major (ldb >= K)
+ * Everything else as tg_gemm_f16_epilogue (epi may be NULL for the identity epilogue).
+ */
+tg_status tg_gemm_f16_t(int trans_a, int trans_b, const void* A, const void* B, void* C,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        const tg_epilogue* epi, const tg_options* opt, tg_stream_t stream);
+
+/*
+ * Backward of the relu epilogue on its fp16 output C: dZ[i,j] = C[i,j] > 0 ? dC[i,j] : +0
+ * (M x N, each with its own leading dimension).  Device pointers, 2-byte aligned;
+ * asynchronous on `stream`.  With dZ, dA = dZ·B^T (tg_gemm_f16_t(0, 1, ...)) and
+ * dB = A^T·dZ (tg_gemm_f16_t(1, 0, ...)).
+ */
+tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t M, int64_t N,
+                               int64_t lddc, int64_t ldc, int64_t lddz, tg_stream_t stream);
+
+/*
  * The plan tg_gemm_relu_f16_ex would use for these arguments on a device with num_sms SMs.
  * The pointers are used only for their alignment.  Pure host function.
  */

@@ -161,6 +161,30 @@ def gemm_epilogue(A, B, act="none", bias=None, residual=None, rows=None, cols=No
     return {"out16_f32acc": o32, "out16_f64acc": o64, "pre_f64": pre}
 
 
+def relu_backward(dC, C) -> np.ndarray:
+    """dZ = C > 0 ? dC : +0 elementwise, on fp16 arrays (returns fp16 bits).  The relu
+    derivative is taken on the forward output C (the practitioner page, section 3.3, asks
+    for a hand-written backward behind torch.autograd.Function); -0 and NaN in C count as
+    not positive."""
+    dC = np.ascontiguousarray(dC, dtype=np.float16)
+    C = np.ascontiguousarray(C, dtype=np.float16)
+    if dC.shape != C.shape:
+        raise ValueError("dC and C must have the same shape")
+    with np.errstate(invalid="ignore"):
+        pos = C > np.float16(0)
+    return np.where(pos, dC.view(np.uint16), np.uint16(0)).astype(np.uint16)
+
+
+def relu_matmul_backward(A, B, C, dC) -> dict:
+    """Gradients of C = relu(A·B) for an incoming dC: dZ = relu_backward(dC, C),
+    dA = dZ·B^T and dB = A^T·dZ, each GEMM as the forward oracle (float32 / float64 sums,
+    one rounding to fp16).  Transposes are data movement only."""
+    dZ = relu_backward(dC, C).view(np.float16)
+    dA = gemm_relu(dZ, np.ascontiguousarray(np.asarray(B, np.float16).T), relu=False)
+    dB = gemm_relu(np.ascontiguousarray(np.asarray(A, np.float16).T), dZ, relu=False)
+    return {"dZ": dZ.view(np.uint16), "dA": dA, "dB": dB}
+
+
 def timed_rows(A, B, nrows: int, relu: bool = True, threads: int = 0):
     """Time the float32-accumulating oracle on the first ``nrows`` rows of C (a bounded
     sample of the whole product).  Returns (seconds, flops, threads_used)."""
