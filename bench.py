@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
                     help="backward: one step = dZ = relu'(C) * dC, dA = dZ B^T, dB = A^T dZ "
                          "(4MNK flops), all in the library's kernels")
+    ap.add_argument("--dequant", default="none", choices=["none", "w4"],
+                    help="w4: B is int4 weights (group 128 scales) decoded inside the GEMM")
     ap.add_argument("--epilogue", default="relu", choices=["relu", "bias_gelu", "bias_relu_residual"],
                     help="relu: the metric's path; the others time the fused bias/GELU/residual "
                          "epilogue on the same GEMM")
@@ -273,16 +275,32 @@ def run_ours(args, wl):
     C = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
     plan = tg.plan(wl.M, wl.N, wl.K, num_sms=props.multi_processor_count,
                    a_ptr=A.data_ptr(), b_ptr=B.data_ptr(), c_ptr=C.data_ptr())
-    in_bytes = (wl.M * wl.K + wl.K * wl.N) * 2
-    flush = in_bytes <= L2_BYTES
-    scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
 
     stream = torch.cuda.Stream(dev)
     handle = stream.cuda_stream
     lib = binding.load_library()
 
     flops_per_step = wl.flops
-    if args.pass_ == "backward":
+    alg_bytes = wl.algorithmic_bytes
+    if args.dequant == "w4":
+        from fp16_gemm_relu_gb300 import inputs as _inputs
+
+        G = 128
+        ldq = -(-(-(-wl.N // 8)) // 4) * 4
+        Wq = torch.from_numpy(_inputs.int4_weights(wl.K, wl.N, wl.seed, ldq=ldq).view(np.int32)).to(dev)
+        Sc = torch.from_numpy(_inputs.int4_scales(-(-wl.K // G), wl.N, wl.seed,
+                                                  1.0 / np.sqrt(wl.K))).to(dev)
+        del B
+        alg_bytes = 2 * wl.M * wl.K + wl.K * wl.N // 2 + 2 * wl.N * (-(-wl.K // G)) + 2 * wl.M * wl.N
+        plan = {**plan, "kernels": 1, "dequant": "w4 g128"}
+
+        def step():
+            st = lib.tg_gemm_w4a16_f16(A.data_ptr(), Wq.data_ptr(), Sc.data_ptr(), C.data_ptr(),
+                                       wl.M, wl.N, wl.K, wl.K, ldq, wl.N, wl.N, G, None, None,
+                                       handle)
+            if st != 0:
+                raise binding.TgError(st, "tg_gemm_w4a16_f16")
+    elif args.pass_ == "backward":
         # gradients of C = relu(A·B) for a seeded dC; the step is mask + two GEMMs
         from fp16_gemm_relu_gb300 import inputs as _inputs
 
@@ -332,6 +350,11 @@ def run_ours(args, wl):
             if st != 0:
                 raise binding.TgError(st, "tg_gemm_f16_epilogue")
 
+    # operand bytes the step reads; below the L2 size, L2 is flushed between timed steps
+    in_bytes = alg_bytes - 2 * wl.M * wl.N
+    flush = in_bytes <= L2_BYTES
+    scrub = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev) if flush else None
+
     bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
     sampler = ClockSampler(bus)
     with torch.cuda.stream(stream):
@@ -379,13 +402,13 @@ def run_ours(args, wl):
     peaks, peak_src = load_peaks()
     kernel_ms = statistics.mean(step_ms)
     t_tensor = wl.flops / (peaks["bf16_tflops"] * FP16_OVER_BF16 * 1e12)
-    t_hbm = wl.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
     if t_tensor >= t_hbm:
         achieved = flops_per_step / (kernel_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved,
                 "peak": peaks["bf16_tflops"] * FP16_OVER_BF16, "unit": "TFLOP/s"}
     else:
-        achieved = wl.algorithmic_bytes / (kernel_ms * 1e-3) / 1e9
+        achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = traffic_from_profiles(wl.name) if plan["kernels"] == 1 else None
@@ -407,7 +430,7 @@ def run_ours(args, wl):
         "data": "synthetic (seeded SplitMix64 inputs of the workload's distribution)",
         "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                    "accumulate": "f32", "output": "f16", "epilogue": args.epilogue,
-                   "pass": args.pass_,
+                   "pass": args.pass_, "dequant": args.dequant,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed between steps" if flush else
                          f"inputs ({in_bytes / 2**20:.0f} MiB) larger than L2",
@@ -418,7 +441,7 @@ def run_ours(args, wl):
         "clocks": sampler.summary(),
     }
 
-    if rank == 0 and not args.no_e2e and args.pass_ == "forward":
+    if rank == 0 and not args.no_e2e and args.pass_ == "forward" and args.dequant == "none":
         line["e2e"] = e2e(wl, A_h, B_h, dev, max(3, min(args.steps, 10)))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, a_np, b_np, args.cpu_seconds)

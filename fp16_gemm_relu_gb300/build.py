@@ -21,8 +21,8 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libtg_gemm_relu.so")
 
 SOURCES = ["tg_api.cu", "tg_gemm_bn256.cu", "tg_gemm_bn192.cu", "tg_gemm_bn128.cu",
-           "tg_gemm_pair.cu", "tg_no_alloc.cu"]
-HEADERS = ["tg_gemm_kernel.cuh", "tg_internal.h"]
+           "tg_gemm_pair.cu", "tg_gemm_w4.cu", "tg_no_alloc.cu"]
+HEADERS = ["tg_gemm_kernel.cuh", "tg_gemm_w4.cuh", "tg_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -556,6 +556,15 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
 namespace tg {
 // Hooks for other translation units of this library (not part of the C ABI).
+tg_status device_info(int* sm_count, unsigned int** err) {
+  DeviceState* ds = nullptr;
+  tg_status st = current_device(&ds);
+  if (st != TG_OK) return st;
+  *sm_count = ds->sm_count;
+  *err = ds->err;
+  return TG_OK;
+}
+
 cudaError_t error_word_address(unsigned int** out) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_tg_error_word);
 }

@@ -55,6 +55,7 @@ struct GemmParams {
   int act;             // epilogue activation: kActNone, kActRelu, kActGelu, kActGeluTanh
   int a_mn;            // 1: A is stored K x M (M contiguous): MN-major tiles, two 64-wide boxes
   int b_k;             // 1: B is stored N x K (K contiguous): K-major tiles, one {64, rows} box
+  int group_kb;        // int4-weight kernel only: k-blocks per scale group
   int debug_flags;
   unsigned long long timeout_ns;
   unsigned int* err;

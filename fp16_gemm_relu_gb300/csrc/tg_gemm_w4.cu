@@ -1,0 +1,127 @@
+// tg_gemm_w4a16_f16: the int4-weight dequantising GEMM (see tg_gemm_w4.cuh for the kernel).
+#include <algorithm>
+#include <cstring>
+
+#include "tg_gemm_w4.cuh"
+#include "tg_internal.h"
+
+namespace {
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+template <int BN>
+cudaError_t launch_w4(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
+                      const CUtensorMap& out, const tg::GemmParams& p, int grid,
+                      cudaStream_t stream) {
+  auto kern = tg::tg_gemm_w4_kernel<BN>;
+  constexpr int smem = tg::W4Cfg<BN>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, tg::kW4Threads, smem, stream>>>(a, q, s, out, p);
+  return cudaGetLastError();
+}
+
+CUresult encode(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, CUtensorMapDataType dt,
+                const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales,
+                                       void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                       int64_t ldq, int64_t lds, int64_t ldc, int group_size,
+                                       const tg_epilogue* epi, const tg_options* opt,
+                                       tg_stream_t stream_) {
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int64_t max_dim = (int64_t{1} << 31) - 1024;
+  if (M < 0 || N < 0 || K < 0 || M > max_dim || N > max_dim || K > max_dim)
+    return TG_ERR_INVALID_ARG;
+  if (group_size < 64 || group_size % 64 != 0) return TG_ERR_INVALID_ARG;
+  if (lda < std::max<int64_t>(1, K) || ldq < cdiv(N, 8) || lds < std::max<int64_t>(1, N) ||
+      ldc < std::max<int64_t>(1, N))
+    return TG_ERR_INVALID_ARG;
+  tg_epilogue e;
+  std::memset(&e, 0, sizeof(e));
+  if (epi) e = *epi;
+  if (e.activation < TG_ACT_NONE || e.activation > TG_ACT_GELU_TANH) return TG_ERR_INVALID_ARG;
+  if (e.residual && (e.ldr < std::max<int64_t>(1, N) || (e.residual == C && e.ldr != ldc)))
+    return TG_ERR_INVALID_ARG;
+  tg_options o;
+  std::memset(&o, 0, sizeof(o));
+  if (opt) o = *opt;
+  if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256) return TG_ERR_INVALID_ARG;
+  if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0) return TG_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return TG_OK;
+  if (C == nullptr) return TG_ERR_INVALID_ARG;
+  if (K == 0)  // no weights are read: the empty sum through the ordinary entry point
+    return tg_gemm_f16_epilogue(nullptr, nullptr, C, M, N, 0, 1, N, ldc, &e, nullptr, stream_);
+  if (!A || !Wq || !scales) return TG_ERR_INVALID_ARG;
+  const uintptr_t bits = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Wq) |
+                         reinterpret_cast<uintptr_t>(scales) | reinterpret_cast<uintptr_t>(C);
+  if ((bits & 15u) || lda % 8 || ldq % 4 || lds % 8 || ldc % 8) return TG_ERR_MISALIGNED;
+  if ((reinterpret_cast<uintptr_t>(e.bias) | reinterpret_cast<uintptr_t>(e.residual)) & 1u)
+    return TG_ERR_MISALIGNED;
+
+  int sms = 0;
+  unsigned int* err = nullptr;
+  tg_status st = tg::device_info(&sms, &err);
+  if (st != TG_OK) return st;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  if (!tg::tensor_map_encoder(&enc)) return TG_ERR_CUDA;
+
+  const int64_t tiles_m = cdiv(M, tg::kBM);
+  int bn = o.block_n;
+  if (bn == 0) bn = (tiles_m * cdiv(N, 256) >= (9 * sms) / 10) ? 256 : 128;
+  const int64_t tiles_n = cdiv(N, bn);
+  const int64_t units = tiles_m * tiles_n;
+  if (units >= (int64_t{1} << 31)) return TG_ERR_INVALID_ARG;
+  const int grid_cap = o.max_ctas > 0 ? std::min(o.max_ctas, sms) : sms;
+
+  CUtensorMap ta, tq, ts, tc;
+  if (encode(enc, &ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, uint64_t(K), uint64_t(M),
+             uint64_t(lda) * 2, tg::kBK, tg::kBM, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+      encode(enc, &tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, uint64_t(cdiv(N, 8)), uint64_t(K),
+             uint64_t(ldq) * 4, uint32_t(bn / 8), tg::kBK, CU_TENSOR_MAP_SWIZZLE_NONE) !=
+          CUDA_SUCCESS ||
+      encode(enc, &ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N),
+             uint64_t(cdiv(K, group_size)), uint64_t(lds) * 2, uint32_t(bn), 1,
+             CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+      encode(enc, &tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C,
+             uint64_t(std::max<int64_t>(N & ~int64_t{7}, 8)), uint64_t(M), uint64_t(ldc) * 2, 64,
+             32, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+    return TG_ERR_CUDA;
+
+  tg::GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.tiles_m = static_cast<int>(tiles_m);
+  p.tiles_n = static_cast<int>(tiles_n);
+  p.num_kb = static_cast<int>(cdiv(K, tg::kBK));
+  p.kb_per_split = p.num_kb;
+  p.splits = 1;
+  p.units = static_cast<int>(units);
+  p.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : 16, tiles_m));
+  p.act = e.activation;
+  p.group_kb = group_size / tg::kBK;
+  p.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : 2000);
+  p.err = err;
+  p.c = static_cast<__half*>(C);
+  p.ldc = ldc;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.n_tma = static_cast<int>(N & ~int64_t{7});
+  p.bias = static_cast<const __half*>(e.bias);
+  p.residual = static_cast<const __half*>(e.residual);
+  p.ldr = e.residual ? e.ldr : 0;
+  const int grid = static_cast<int>(std::min<int64_t>(units, grid_cap));
+  const cudaError_t ce = bn == 256 ? launch_w4<256>(ta, tq, ts, tc, p, grid, stream)
+                                   : launch_w4<128>(ta, tq, ts, tc, p, grid, stream);
+  return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+}

@@ -1,0 +1,276 @@
+// tg_gemm_w4.cuh — C = epilogue(A · dequant(Wq)) with fp16 activations A (M x K) and 4-bit
+// integer weights (the W_INT4 / A_FP16 dequantising GEMM of the TileLang paper-reading page,
+// section 5), on the same tcgen05 main loop as tg_gemm_tc_kernel.
+//
+// Weight format: Wq is K rows of ceil(N/8) uint32 words; word (k, c) carries columns
+// 8c..8c+7, column 8c+e in bits [4e, 4e+4), unsigned q in [0, 15] with zero point 8.  scales
+// is ceil(K/G) rows of N fp16 values, G a multiple of 64.  w[k][n] = fp16((q - 8) * s[k/G][n]),
+// the product rounded once (fp16 subtract of 1032 from the exact 1024 + q, then an fp16
+// multiply: both IEEE round-to-nearest-even).
+//
+// Warp roles (320 threads):
+//   warp 0     TMA: per stage the A tile, the packed Wq tile (64 rows x BN/8 words) and the
+//              group's scale row (BN fp16), all on one load_full barrier.
+//   warp 1     tcgen05.mma issuer; waits for load_full (A) and deq_full (decoded B).
+//   warps 2-5  epilogue (shared with the fp16 kernels).
+//   warps 6-9  dequantisers: read packed words and scales from shared memory, decode eight
+//              weights per word in registers and store them as the 128B-swizzled MN-major B
+//              tile the MMA expects; then fence.proxy.async and arrive on deq_full.
+// TMA zero fill makes the tails safe: scales past N or past the last group are 0, so those
+// weights decode to 0 whatever their nibbles.
+#pragma once
+
+#include "tg_gemm_kernel.cuh"
+
+namespace tg {
+
+constexpr int kW4Threads = 320;
+constexpr int kDeqWarps = 4;
+
+template <int BN>
+struct W4Cfg {
+  static constexpr int kAStage = kBM * kBK * 2;   // 16 KB fp16 A
+  static constexpr int kBStage = kBK * BN * 2;    // decoded fp16 B tile
+  static constexpr int kQStage = kBK * BN / 2;    // packed int4 tile
+  static constexpr int kSStage = 1024;            // one scale row (BN fp16), padded
+  static constexpr int kStageBytes = kAStage + kBStage + kQStage + kSStage;
+  static constexpr int kTxBytes = kAStage + kQStage + BN * 2;
+  static constexpr int kStagingBytes = kEpiWarps * 2 * kStagingBuf;
+  static constexpr int kStagesFit = (kSmemLimit - kSmemReserve - kStagingBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kAccStride = BN <= 128 ? 128 : 256;
+  static constexpr int kTmemCols = 2 * kAccStride;
+  static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes + kStagingBytes;
+  static_assert(kStages >= 2, "not enough shared memory");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
+};
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  return __byte_perm(a, b, sel);
+}
+
+// Eight weights of one packed word; sp[e] holds the scales of columns (e, e+4).  Returns the
+// fp16 weights of columns 0..7 in order, two per 32-bit word.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, const uint32_t (&sp)[4]) {
+  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  uint32_t pr[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t x = ((w >> (4 * e)) & 0x000F000Fu) | 0x64006400u;  // (1024+q_e, 1024+q_e+4)
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), k1032);  // q - 8, exact
+    h = __hmul2(h, *reinterpret_cast<const __half2*>(&sp[e]));        // one rounding
+    pr[e] = *reinterpret_cast<uint32_t*>(&h);                          // columns (e, e+4)
+  }
+  return make_uint4(prmt(pr[0], pr[1], 0x5410), prmt(pr[2], pr[3], 0x5410),
+                    prmt(pr[0], pr[1], 0x7632), prmt(pr[2], pr[3], 0x7632));
+}
+
+// tmA: fp16 A {K, M} box {64, 128} SW128; tmQ: uint32 Wq {ceil(N/8), K} box {BN/8, 64};
+// tmS: fp16 scales {N, ceil(K/G)} box {BN, 1}; tmOut: fp16 C {n_tma, M} box {64, 32} SW128.
+// p.splits must be 1; p.kb_per_split = p.num_kb; p.group_kb = G / 64.
+template <int BN>
+__global__ void __launch_bounds__(kW4Threads, 1)
+    tg_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmS,
+                      const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  using Cfg = W4Cfg<BN>;
+  constexpr int S = Cfg::kStages;
+  constexpr int W = BN / 8;  // packed words per row
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * Cfg::kAStage;
+  uint8_t* sQ = sB + S * Cfg::kBStage;
+  uint8_t* sS = sQ + S * Cfg::kQStage;
+  uint8_t* sStg = sS + S * Cfg::kSStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStagingBytes);
+  uint64_t* load_full = bars;
+  uint64_t* deq_full = bars + S;
+  uint64_t* empty = bars + 2 * S;
+  uint64_t* tfull = bars + 3 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&load_full[s]), 1);
+      mbar_init(smem_u32(&deq_full[s]), kDeqWarps);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmS);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
+            goto w4_producer_done;
+          const uint32_t fb = smem_u32(&load_full[stage]);
+          mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+          tma_load_2d(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, w.m_blk * kBM);
+          tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
+          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * BN,
+                      kb / p.group_kb);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    w4_producer_done:
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) wait_phase_drain(smem_u32(&load_full[s]), (armed_parity >> s) & 1u, p);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(kBM, BN, 0, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+        const Unit w = unit_of(p, u);
+        const int buf = t & 1;
+        const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+        if (!wait_phase(smem_u32(&tempty[buf]), use ^ 1u, abort_flag, p, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        bool ok = true;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&load_full[stage]), phase, abort_flag, p, kRoleMma) ||
+              !wait_phase(smem_u32(&deq_full[stage]), phase, abort_flag, p, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_kmajor(smem_u32(sA + stage * Cfg::kAStage));
+          const uint64_t bd = desc_mnmajor(smem_u32(sB + stage * Cfg::kBStage));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16(d_tmem, ad + 2u * k, bd + 128u * k, idesc, (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[stage]));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[buf]));
+      }
+      umma_commit(smem_u32(drain));
+      wait_phase_drain(smem_u32(drain), 0u, p);
+    }
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------ epilogue ------------------------------
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    uint8_t* stg = sStg + ew * 2 * kStagingBuf;
+    int sb = 0;
+    int t = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+      const Unit w = unit_of(p, u);
+      const int buf = t & 1;
+      const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * Cfg::kAccStride);
+      epilogue_tile<BN, false>(&tmOut, p, tl, w.m_blk * kBM + q * 32, w.n_blk * BN, 0, stg, sb,
+                               smem_u32(&tempty[buf]), false, lane);
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  } else {
+    // ------------------------------ dequantisers ------------------------------
+    const int dt = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 127
+    const int cw = dt % W;                               // packed word column
+    const int row_first = dt / W;
+    constexpr int kRowStep = 128 / W;
+    const int box = cw / 8, chunk = cw % 8;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const Unit w = unit_of(p, u);
+      bool ok = true;
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        int ready = 0;
+        if (lane == 0)
+          ready = wait_phase(smem_u32(&load_full[stage]), phase, abort_flag, p, kRoleProducer);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (!ready) {
+          ok = false;
+          break;
+        }
+        // the eight scales of this thread's columns, paired (e, e+4) like dequant8's halves
+        const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
+        const uint32_t sp[4] = {prmt(sv.x, sv.z, 0x5410), prmt(sv.x, sv.z, 0x7632),
+                                prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
+        const uint32_t* q = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
+        uint8_t* bdst = sB + stage * Cfg::kBStage + box * 8192;
+#pragma unroll 4
+        for (int i = 0; i < 64 / kRowStep; ++i) {
+          const int r = row_first + i * kRowStep;
+          const uint4 v = dequant8(q[r * W + cw], sp);
+          *reinterpret_cast<uint4*>(bdst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&deq_full[stage]));
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace tg

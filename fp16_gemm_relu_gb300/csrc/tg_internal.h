@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "tg_gemm_kernel.cuh"
+#include "tg_gemm_relu.h"
 
 namespace tg {
 
@@ -30,6 +31,9 @@ cudaError_t launch_gemm_bn128(const GemmLaunch& l, bool out_f32);
 cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32);
 // Clusters of two that can be resident at once on the current device.
 cudaError_t gemm_pair_max_clusters(int* out);
+
+// Current device's SM count and error word (checks the device; sets up library state).
+tg_status device_info(int* sm_count, unsigned int** err);
 
 // Address of the device error word that kernels set when a pipeline wait runs out.
 cudaError_t error_word_address(unsigned int** out);

@@ -99,3 +99,34 @@ def embed(x: np.ndarray, ld: int, fill: float = 0.0) -> np.ndarray:
     buf = np.full((rows, ld), fill, dtype=x.dtype)
     buf[:, :cols] = x
     return buf
+
+
+def int4_weights(K: int, N: int, seed: int, ldq: int | None = None) -> np.ndarray:
+    """Packed 4-bit weights: K rows of ldq (>= ceil(N/8)) uint32 words; nibble e of word c is
+    column 8c+e, each nibble uniform in [0, 15] from the stream (seed, tensor 2); words past
+    ceil(N/8) and nibbles past column N are zero."""
+    words = (N + 7) // 8
+    ldq = words if ldq is None else ldq
+    if ldq < words:
+        raise ValueError("ldq < ceil(N/8)")
+    k0 = stream_key(seed, 2, 0)
+    out = np.zeros((K, ldq), dtype=np.uint32)
+    nib = np.empty((K, words * 8), dtype=np.uint32)
+    flat = (raw_u64(k0, 0, K * N) >> np.uint64(60)).astype(np.uint32).reshape(K, N)
+    nib[:, :N] = flat
+    nib[:, N:] = 0
+    nib = nib.reshape(K, words, 8)
+    packed = np.zeros((K, words), dtype=np.uint32)
+    for e in range(8):
+        packed |= nib[:, :, e] << np.uint32(4 * e)
+    out[:, :words] = packed
+    return out
+
+
+def int4_scales(groups: int, N: int, seed: int, scale: float, lds: int | None = None) -> np.ndarray:
+    """fp16 group scales, groups x lds (>= N): uniform in [0.5, 1.5) x scale, rounded once."""
+    lds = N if lds is None else lds
+    s = tensor(groups, N, seed, 3, "uniform", 1.0).astype(np.float64) * 0.5 + 1.0
+    out = np.zeros((groups, lds), dtype=np.float16)
+    out[:, :N] = (s * scale).astype(np.float16)
+    return out

@@ -155,6 +155,25 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
                                int64_t lddc, int64_t ldc, int64_t lddz, tg_stream_t stream);
 
 /*
+ * Dequantising GEMM with 4-bit integer weights and fp16 activations (the W_INT4 / A_FP16
+ * case of the TileLang paper-reading page, section 5):
+ *     C = fp16( epilogue( A · W ) ),   W[k][n] = fp16( (q[k][n] - 8) * scales[k / G][n] )
+ * A: device fp16 M x K row-major, 16-byte aligned, lda a multiple of 8.
+ * Wq: device uint32, K rows of ldq words (ldq >= ceil(N/8), multiple of 4, 16-byte aligned);
+ *     word (k, c) holds columns 8c..8c+7, column 8c+e in bits [4e, 4e+4), q unsigned 0..15.
+ * scales: device fp16, ceil(K/G) rows of lds values (lds >= N, multiple of 8, 16-byte
+ *     aligned).  group_size G: a multiple of 64.
+ * C: device fp16 M x N, 16-byte aligned, ldc a multiple of 8.  epi as tg_gemm_f16_epilogue.
+ * The weights are decoded inside the GEMM kernel (never written to memory).  opt may set
+ * block_n (128 or 256), max_ctas, panel_m and timeout_ms.  Misaligned arguments return
+ * TG_ERR_MISALIGNED; asynchronous on `stream`.
+ */
+tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales, void* C,
+                            int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldq,
+                            int64_t lds, int64_t ldc, int group_size, const tg_epilogue* epi,
+                            const tg_options* opt, tg_stream_t stream);
+
+/*
  * The plan tg_gemm_relu_f16_ex would use for these arguments on a device with num_sms SMs.
  * The pointers are used only for their alignment.  Pure host function.
  */

@@ -43,6 +43,8 @@ def lib() -> ctypes.CDLL:
         L.tg_oracle_gemm_epilogue.restype = ctypes.c_int
         L.tg_oracle_gemm_epilogue.argtypes = [p, p, i64, i64, i64, i64, i64, p, i64, p, i64,
                                               ctypes.c_int, p, p, i64, p, p, p, ctypes.c_int]
+        L.tg_oracle_dequant_w4.restype = ctypes.c_int
+        L.tg_oracle_dequant_w4.argtypes = [p, p, i64, i64, i64, i64, i64, p]
         L.tg_oracle_max_threads.restype = ctypes.c_int
         L.tg_oracle_max_threads.argtypes = []
         _lib = L
@@ -159,6 +161,19 @@ def gemm_epilogue(A, B, act="none", bias=None, residual=None, rows=None, cols=No
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return {"out16_f32acc": o32, "out16_f64acc": o64, "pre_f64": pre}
+
+
+def dequant_w4(Wq, scales, K: int, N: int, group: int) -> np.ndarray:
+    """fp16 K x N weights from packed int4 Wq (K x ceil(N/8) uint32) and fp16 scales
+    (ceil(K/group) x N): w = fp16_rne((q - 8) * s).  See tg_oracle.c for the format."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
+    sc = np.ascontiguousarray(scales, dtype=np.float16).view(np.uint16)
+    out = np.empty((K, N), np.uint16)
+    rc = lib().tg_oracle_dequant_w4(_ptr(Wq), _ptr(sc), K, N, Wq.shape[1], sc.shape[1], group,
+                                    _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out.view(np.float16)
 
 
 def relu_backward(dC, C) -> np.ndarray:

@@ -235,3 +235,27 @@ int tg_oracle_gemm_epilogue(const uint16_t* A, const uint16_t* B, int64_t M, int
   free(s64);
   return rc;
 }
+
+/* ---- int4 weight dequantisation (W_INT4 / A_FP16 GEMM) ----
+ *
+ * The paper-reading page (section 5) evaluates a dequantising GEMM with 4-bit integer weights
+ * and fp16 activations.  Format used here: Wq holds K rows of ceil(N/8) uint32 words; word
+ * (k, c) carries columns 8c..8c+7, column 8c+e in bits [4e, 4e+4); q is unsigned in [0, 15]
+ * with the zero point 8.  scales holds ceil(K/group) rows of N fp16 values (leading dimension
+ * lds).  The weight is
+ *     w[k][n] = fp16_rne( (q[k][n] - 8) * scales[k / group][n] )
+ * (the product is exact in double; one rounding).  out16 is K x N fp16 bits, row-major.
+ */
+int tg_oracle_dequant_w4(const uint32_t* Wq, const uint16_t* scales, int64_t K, int64_t N,
+                         int64_t ldq, int64_t lds, int64_t group, uint16_t* out16) {
+  if (K < 0 || N < 0 || group <= 0 || ldq < (N + 7) / 8 || lds < N) return -1;
+  for (int64_t k = 0; k < K; ++k) {
+    for (int64_t n = 0; n < N; ++n) {
+      const uint32_t word = Wq[k * ldq + n / 8];
+      const int q = (int)((word >> (4 * (n % 8))) & 0xFu);
+      const double s = tg_oracle_f16_to_f64(scales[(k / group) * lds + n]);
+      out16[k * N + n] = tg_oracle_f64_to_f16((double)(q - 8) * s);
+    }
+  }
+  return 0;
+}

@@ -143,3 +143,19 @@ def test_epilogue_argument_errors(lib):
     assert e(p, p, p, 4, 4, 4, 4, 4, 4, 1, 0, p, 3) == binding.TG_ERR_INVALID_ARG  # ldr < N
     assert e(p, p, p, 4, 4, 4, 4, 4, 8, 1, 0, p, 4) == binding.TG_ERR_INVALID_ARG  # C alias, ldr != ldc
     assert e(0, 0, 0, 0, 4, 4, 4, 4, 4, 2) == binding.TG_OK                       # empty
+
+
+def test_w4_argument_errors(lib):
+    p = 4096
+    def call(*a):
+        args = [p, p, p, p, 64, 64, 64, 64, 8, 64, 64, 128]
+        for i, v in a:
+            args[i] = v
+        return binding.tg_gemm_w4a16_f16(*args)
+    assert call() == binding.TG_ERR_UNSUPPORTED_DEVICE or call() in (binding.TG_ERR_CUDA, binding.TG_OK)
+    assert call((11, 96)) == binding.TG_ERR_INVALID_ARG     # group size not a multiple of 64
+    assert call((8, 7)) == binding.TG_ERR_INVALID_ARG       # ldq < ceil(N/8)
+    assert call((9, 60)) == binding.TG_ERR_INVALID_ARG      # lds < N
+    assert call((8, 10)) == binding.TG_ERR_MISALIGNED       # ldq not a multiple of 4
+    assert call((1, p + 4)) == binding.TG_ERR_MISALIGNED    # Wq not 16-byte aligned
+    assert call((4, 0)) == binding.TG_OK                    # M == 0

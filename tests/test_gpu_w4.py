@@ -1,0 +1,104 @@
+"""Parity of the int4-weight dequantising GEMM (tg_gemm_w4a16_f16) with the oracle:
+oracle.dequant_w4 decodes the weights, oracle.gemm_epilogue multiplies; ragged M/N/K
+(partial last scale group, N not a multiple of 8), both tile widths, multi-tile CTAs, the
+fused epilogues and the decode-like shape on sampled outputs."""
+
+import numpy as np
+import pytest
+
+import oracle
+from fp16_gemm_relu_gb300 import binding, inputs
+
+from tests.parity import compare
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from fp16_gemm_relu_gb300 import build
+
+    build.build()
+    binding.load_library()
+    torch.cuda.set_device(0)
+    yield
+    st, word = binding.tg_device_error_check(clear=True)
+    assert st == binding.TG_OK, f"device error word {word:#x}"
+
+
+def run_w4(a, Wq, S, N, G, act=0, bias=None, residual=None, options=None):
+    M, K = a.shape
+    A = torch.from_numpy(inputs.embed(a, -(-K // 8) * 8)).cuda()
+    Q = torch.from_numpy(Wq.view(np.int32)).cuda()
+    Sc = torch.from_numpy(S).cuda()
+    ldc = -(-N // 8) * 8
+    C = torch.full((M, ldc), float("nan"), dtype=torch.float16, device="cuda")
+    b = torch.from_numpy(bias).cuda() if bias is not None else None
+    r = torch.from_numpy(residual).cuda() if residual is not None else None
+    st = binding.tg_gemm_w4a16_f16(A.data_ptr(), Q.data_ptr(), Sc.data_ptr(), C.data_ptr(), M, N,
+                                   K, A.shape[1], Wq.shape[1], S.shape[1], ldc, G, act,
+                                   b.data_ptr() if b is not None else 0,
+                                   r.data_ptr() if r is not None else 0,
+                                   N if r is not None else 0, options,
+                                   torch.cuda.current_stream().cuda_stream)
+    assert st == binding.TG_OK, binding.tg_status_string(st)
+    torch.cuda.synchronize()
+    out = C.cpu().numpy()
+    assert np.isnan(out[:, N:]).all()
+    return out[:, :N].view(np.uint16)
+
+
+def make(M, N, K, G, seed, scale=None):
+    a = inputs.tensor(M, K, seed, 0)
+    ldq = -(-(-(-N // 8)) // 4) * 4
+    Wq = inputs.int4_weights(K, N, seed, ldq=ldq)
+    S = inputs.int4_scales(-(-K // G), N, seed, scale or 1.0 / np.sqrt(K), lds=-(-N // 8) * 8)
+    return a, Wq, S
+
+
+def check(got, a, Wq, S, N, G, act="none", bias=None, residual=None, rows=None, cols=None):
+    K = a.shape[1]
+    w = oracle.dequant_w4(Wq, S, K, N, G)
+    r = oracle.gemm_epilogue(a, w, act, bias=bias, residual=residual, rows=rows, cols=cols)
+    ref = {"out16_f64acc": r["out16_f64acc"], "acc_f64": r["pre_f64"]}
+    zr = act == "relu" and residual is None
+    c = compare(got, ref, K, relu=zr)
+    assert c["out_of_tol"] == 0 and (not zr or c["zero_rule"] == 0), c
+    return c
+
+
+@pytest.mark.parametrize("M,N,K,G", [(128, 256, 128, 64), (333, 527, 1030, 128),
+                                     (64, 1000, 4096, 128), (700, 300, 640, 256)])
+@pytest.mark.parametrize("bn", [128, 256])
+def test_w4_parity(M, N, K, G, bn):
+    a, Wq, S = make(M, N, K, G, 7)
+    got = run_w4(a, Wq, S, N, G, options={"block_n": bn})
+    check(got, a, Wq, S, N, G)
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu"])
+def test_w4_epilogue_and_multitile(act):
+    M, N, K, G = 400, 600, 1024, 128
+    a, Wq, S = make(M, N, K, G, 8)
+    bias = inputs.tensor(1, N, 9, 0).ravel()
+    res = inputs.tensor(M, N, 9, 1)
+    ACT = {"relu": 1, "gelu": 2}
+    got = run_w4(a, Wq, S, N, G, act=ACT[act], bias=bias, residual=res,
+                 options={"max_ctas": 3, "block_n": 128})
+    check(got, a, Wq, S, N, G, act, bias, res)
+    got0 = run_w4(a, Wq, S, N, G, act=ACT[act], options={"max_ctas": 2})
+    check(got0, a, Wq, S, N, G, act)
+
+
+def test_w4_decode_shape_sampled():
+    M, N, K, G = 64, 28672, 8192, 128
+    a = inputs.tensor(M, K, 3, 0, "normal")
+    Wq = inputs.int4_weights(K, N, 3)
+    S = inputs.int4_scales(K // G, N, 3, 1.0 / np.sqrt(K))
+    got = run_w4(a, Wq, S, N, G, act=1)
+    rng = np.random.default_rng(0)
+    cols = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 200)]))
+    rows = np.arange(M)
+    check(got[np.ix_(rows, cols)], a, Wq[:, :], S, N, G, "relu", rows=rows, cols=cols)
