@@ -246,10 +246,16 @@ __global__ void __launch_bounds__(kW4Threads, 1)
                                 prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
         const uint32_t* q = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
         uint8_t* bdst = sB + stage * Cfg::kBStage + box * 8192;
-#pragma unroll 4
-        for (int i = 0; i < 64 / kRowStep; ++i) {
+        // all of this thread's words first, then independent decodes: the rows give the
+        // scheduler 64/kRowStep independent chains to interleave
+        constexpr int kRows = 64 / kRowStep;
+        uint32_t words[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) words[i] = q[(row_first + i * kRowStep) * W + cw];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
           const int r = row_first + i * kRowStep;
-          const uint4 v = dequant8(q[r * W + cw], sp);
+          const uint4 v = dequant8(words[i], sp);
           *reinterpret_cast<uint4*>(bdst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
         }
         fence_async_smem();
