@@ -195,6 +195,24 @@ def dist_env():
     return world, rank, local
 
 
+def slowest_rank_ms(total_ms: float, device=None) -> float:
+    """The timed region's length on the slowest rank (all-reduce MAX; the identity without a
+    process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, steps: int, flops_per_step: float, total_ms: float) -> float:
+    """Work of all replicas (each rank runs the full workload) over the slowest rank's time."""
+    return world * steps * flops_per_step / (total_ms * 1e-3) / 1e12
+
+
 def cpu_baseline(wl, a, b, target_s: float, relu=True):
     """The oracle as it stands, on a bounded sample: the first R rows of C."""
     import oracle
@@ -387,12 +405,9 @@ def run_ours(args, wl):
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     region_ms = t_all0.elapsed_time(t_all1)
     total_ms = sum(step_ms) if flush else region_ms
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(total_ms, device=dev)
     ms_per_step = total_ms / args.steps
-    value = world * args.steps * flops_per_step / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, args.steps, flops_per_step, total_ms)
     st, word = binding.tg_device_error_check(clear=True)
     if st != 0:
         raise RuntimeError(f"device error word {word:#x} after the timed region")
