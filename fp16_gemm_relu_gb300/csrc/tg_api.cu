@@ -133,6 +133,7 @@ struct Plan {
   tg_plan pub;
   int64_t lda_p, ldb_p, ldw;     // leading dimensions of the scratch copies / workspace
   int64_t off_a, off_b, off_w;   // byte offsets inside the scratch block
+  int64_t off_tail_ws, off_tail_cnt, tail_cnt_bytes;  // tail-split partials and counters
 };
 
 // Per-k-block cost in SM cycles of an output tile 128 x bn: the tensor-core time (a
@@ -158,7 +159,7 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 192 && o.block_n != 256)
     return TG_ERR_INVALID_ARG;
   if (o.split_k < 0 || o.panel_m < 0 || o.max_ctas < 0 || o.timeout_ms < 0 || o.pair < -1 ||
-      o.pair > 1)
+      o.pair > 1 || o.tail < -1 || o.tail > 1)
     return TG_ERR_INVALID_ARG;
   if (o.pair == 1 && o.block_n != 0 && o.block_n != 256) return TG_ERR_INVALID_ARG;
 
@@ -256,6 +257,16 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
                      : static_cast<int>(std::min<int64_t>(P.units, grid_cap));
   P.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : kDefaultPanel, P.tiles_m));
   P.workspace_epilogue = (P.split_k > 1 || !c_direct) ? 1 : 0;
+  // Tail split: when the last wave of pair tiles would leave more than half the clusters
+  // idle, its r tiles run as 2r K halves instead (each wave before it stays whole).
+  if (P.cta_pair && P.split_k == 1 && !P.workspace_epilogue && o.tail >= 0 && P.kblocks >= 2) {
+    const int64_t clusters = P.grid / 2;
+    const int64_t r = P.units % clusters;
+    if (r > 0 && 2 * r <= clusters && P.units > clusters) {
+      P.tail_tiles = r;
+      P.units += r;
+    }
+  }
 
   int64_t off = 0;
   if (P.repack_a) {  // A is stored (ta ? K x M : M x K)
@@ -272,6 +283,13 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
     pl.ldw = round_up(N, 4);
     pl.off_w = off;
     off += round_up(int64_t(P.split_k) * M * pl.ldw * 4, 256);
+  }
+  if (P.tail_tiles) {
+    pl.off_tail_ws = off;
+    off += round_up(P.tail_tiles * 2 * 256 * 256 * 4, 256);
+    pl.off_tail_cnt = off;
+    pl.tail_cnt_bytes = round_up(P.tail_tiles * 8 * 4, 256);
+    off += pl.tail_cnt_bytes;
   }
   P.workspace_bytes = off;
   P.kernels = 1 + P.repack_a + P.repack_b + P.workspace_epilogue;
@@ -524,6 +542,14 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   gp.ldr = epi.residual ? epi.ldr : 0;
   gp.a_mn = ta;
   gp.b_k = tb;
+  if (P.tail_tiles) {
+    gp.tail = 1;
+    gp.n_full = static_cast<int>(P.units - 2 * P.tail_tiles);
+    gp.tail_ws = reinterpret_cast<float*>(scratch + pl.off_tail_ws);
+    gp.tail_cnt = reinterpret_cast<int*>(scratch + pl.off_tail_cnt);
+    e = cudaMemsetAsync(gp.tail_cnt, 0, size_t(pl.tail_cnt_bytes), stream);
+    if (e != cudaSuccess) return fail(cuda_fail(e));
+  }
   gp.debug_flags = o.debug_flags;
   gp.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : kDefaultTimeoutMs);
   gp.err = ds->err;

@@ -56,6 +56,12 @@ struct GemmParams {
   int a_mn;            // 1: A is stored K x M (M contiguous): MN-major tiles, two 64-wide boxes
   int b_k;             // 1: B is stored N x K (K contiguous): K-major tiles, one {64, rows} box
   int group_kb;        // int4-weight kernel only: k-blocks per scale group
+  // tail split (pair kernel, fp16 output): units [0, n_full) are whole tiles; each of the
+  // remaining tiles is two units, one per K half, that meet through tail_ws / tail_cnt
+  int tail;
+  int n_full;
+  float* tail_ws;      // [slot][half][part = rank*4 + quarter][32 rows][256] float32 partials
+  int* tail_cnt;       // [slot][part] arrival counters, zero before the launch
   int debug_flags;
   unsigned long long timeout_ns;
   unsigned int* err;
@@ -407,16 +413,27 @@ __device__ __forceinline__ uint64_t desc_k_step(int mn_major) { return mn_major 
 // ---------------------------------------------------------------------------------------
 struct Unit {
   int m_blk, n_blk, split, kb_begin, kb_end;
+  int tail_slot;  // -1, or the index of a tail-split tile (split = its K half)
 };
 
 // Unit u -> (split, tile); splits are the outer index so that co-running CTAs share a K range.
 // Tiles walk panels of panel_m M-tiles, M-tile fastest inside a panel (T.use_swizzle-style
 // rasterisation, TileLang paper-reading page, section 4).
+// With p.tail, units past n_full are K halves of the last tiles (tile n_full + slot).
 __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
   Unit w;
   const int tiles = p.tiles_m * p.tiles_n;
-  w.split = u / tiles;
-  const int t = u - w.split * tiles;
+  int t;
+  w.tail_slot = -1;
+  if (p.tail && u >= p.n_full) {
+    const int v = u - p.n_full;
+    w.tail_slot = v >> 1;
+    w.split = v & 1;
+    t = p.n_full + w.tail_slot;
+  } else {
+    w.split = u / tiles;
+    t = u - w.split * tiles;
+  }
   const int group = p.panel_m * p.tiles_n;
   const int g = t / group;
   const int r = t - g * group;
@@ -424,8 +441,14 @@ __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
   const int rows = min(p.panel_m, p.tiles_m - first_m);
   w.m_blk = first_m + r % rows;
   w.n_blk = r / rows;
-  w.kb_begin = w.split * p.kb_per_split;
-  w.kb_end = min(w.kb_begin + p.kb_per_split, p.num_kb);
+  if (w.tail_slot >= 0) {
+    const int half = (p.num_kb + 1) >> 1;
+    w.kb_begin = w.split ? half : 0;
+    w.kb_end = w.split ? p.num_kb : half;
+  } else {
+    w.kb_begin = w.split * p.kb_per_split;
+    w.kb_end = min(w.kb_begin + p.kb_per_split, p.num_kb);
+  }
   return w;
 }
 
@@ -536,6 +559,57 @@ __device__ __forceinline__ void epilogue_general_32(const uint32_t (&acc)[32], i
   }
 }
 
+// 64 columns of one row per lane (float32 bits in r0 = columns 0..31, r1 = 32..63): epilogue,
+// fp16 pack, 128B-swizzled staging and TMA store of the warp's 32 x 64 block; columns in
+// [n_tma, N) are written with plain stores.
+__device__ __forceinline__ void store_chunk_f16(const CUtensorMap* tmOut, const GemmParams& p,
+                                                const uint32_t (&r0)[32],
+                                                const uint32_t (&r1)[32], int row0, int col0,
+                                                uint8_t* stg, int& sb, int lane) {
+  uint32_t pk[32];
+  if (p.bias == nullptr && p.residual == nullptr && p.act <= kActRelu) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.act);
+      pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.act);
+    }
+  } else {
+    // general fused epilogue, 32 columns at a time; columns past N and rows past M are
+    // computed but never stored
+    epilogue_general_32(r0, row0 + lane, col0, p, pk);
+    epilogue_general_32(r1, row0 + lane, col0 + 32, p, pk + 16);
+  }
+  if (col0 < p.n_tma) {
+    uint8_t* st = stg + sb * kStagingBuf;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmOut, smem_u32(st), col0, row0);
+      bulk_commit();
+    }
+    sb ^= 1;
+  }
+  if (col0 + 64 > p.n_tma && col0 < p.N && row0 + lane < p.M) {
+    // ragged tail columns [n_tma, N): plain 2-byte stores of this thread's row
+    const int jb = max(p.n_tma, col0) - col0;
+    const int je = min(p.N, col0 + 64) - col0;
+    unsigned short* dst = reinterpret_cast<unsigned short*>(p.c) +
+                          static_cast<long long>(row0 + lane) * p.ldc + col0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (2 * i >= jb && 2 * i < je) dst[2 * i] = static_cast<unsigned short>(pk[i] & 0xFFFFu);
+      if (2 * i + 1 >= jb && 2 * i + 1 < je) dst[2 * i + 1] = static_cast<unsigned short>(pk[i] >> 16);
+    }
+  }
+}
+
 // One output tile's epilogue for one warp: TMEM lane quarter at `tl` (32 rows starting at
 // row0, BN columns starting at col_base) -> registers -> epilogue -> 128B-swizzled staging ->
 // TMA store.  After the last tcgen05.ld the warp releases the accumulator by arriving on
@@ -565,49 +639,7 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
       tmem_ld_x32(tl + c * 64 + 32, r1);
       tmem_wait_ld(r1);
       if (c == BN / 64 - 1) release();
-      const int col0 = col_base + c * 64;
-      uint32_t pk[32];
-      if (p.bias == nullptr && p.residual == nullptr && p.act <= kActRelu) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          pk[i] = relu_pack_h2(r0[2 * i], r0[2 * i + 1], p.act);
-          pk[16 + i] = relu_pack_h2(r1[2 * i], r1[2 * i + 1], p.act);
-        }
-      } else {
-        // general fused epilogue, 32 columns at a time; columns past N and rows past M are
-        // computed but never stored
-        epilogue_general_32(r0, row0 + lane, col0, p, pk);
-        epilogue_general_32(r1, row0 + lane, col0 + 32, p, pk + 16);
-      }
-      if (col0 < p.n_tma) {
-        uint8_t* st = stg + sb * kStagingBuf;
-        if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint4 v = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          *reinterpret_cast<uint4*>(st + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(tmOut, smem_u32(st), col0, row0);
-          bulk_commit();
-        }
-        sb ^= 1;
-      }
-      if (col0 + 64 > p.n_tma && col0 < p.N && row0 + lane < p.M) {
-        // ragged tail columns [n_tma, N): plain 2-byte stores of this thread's row
-        const int jb = max(p.n_tma, col0) - col0;
-        const int je = min(p.N, col0 + 64) - col0;
-        unsigned short* dst = reinterpret_cast<unsigned short*>(p.c) +
-                              static_cast<long long>(row0 + lane) * p.ldc + col0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if (2 * i >= jb && 2 * i < je) dst[2 * i] = static_cast<unsigned short>(pk[i] & 0xFFFFu);
-          if (2 * i + 1 >= jb && 2 * i + 1 < je) dst[2 * i + 1] = static_cast<unsigned short>(pk[i] >> 16);
-        }
-      }
+      store_chunk_f16(tmOut, p, r0, r1, row0, col_base + c * 64, stg, sb, lane);
     }
   } else {
 #pragma unroll 1
@@ -818,6 +850,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Epilogue of one K half of a tail-split tile (fp16 output), for one warp of the pair kernel:
+// store this half's float32 rows to tail_ws, then count arrivals on the tile's (rank, quarter)
+// counter.  The warp that arrives second adds the two halves (a + b == b + a in IEEE
+// arithmetic, so the sum does not depend on which half finished last), runs the normal
+// epilogue and resets the counter.  No warp waits for another CTA.
+template <int BN>
+__device__ __forceinline__ void epilogue_tail(const CUtensorMap* tmOut, const GemmParams& p,
+                                              uint32_t tl, int row0, int col_base, int slot,
+                                              int half, int part, uint8_t* stg, int& sb,
+                                              uint32_t release_bar, int lane) {
+  const long long per_part = 32LL * BN;
+  float* mine = p.tail_ws + ((static_cast<long long>(slot) * 2 + half) * 8 + part) * per_part +
+                lane * BN;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld_x32(tl + c * 32, r);
+    tmem_wait_ld(r);
+    if (c == BN / 32 - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(release_bar);
+    }
+    float4* d = reinterpret_cast<float4*>(mine + c * 32);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+  }
+  __threadfence();
+  __syncwarp();
+  int arrived = 0;
+  if (lane == 0) arrived = atomicAdd(p.tail_cnt + slot * 8 + part, 1);
+  arrived = __shfl_sync(0xffffffffu, arrived, 0);
+  if (arrived == 0) return;  // the other half completes this block
+  __threadfence();
+  const float* other = p.tail_ws + ((static_cast<long long>(slot) * 2 + (half ^ 1)) * 8 + part) *
+                                       per_part + lane * BN;
+#pragma unroll 1
+  for (int c = 0; c < BN / 64; ++c) {
+    uint32_t r0[32], r1[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 a = *reinterpret_cast<const float4*>(mine + c * 64 + 4 * j);
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(other + c * 64 + 4 * j));
+      r0[4 * j] = __float_as_uint(a.x + b.x);
+      r0[4 * j + 1] = __float_as_uint(a.y + b.y);
+      r0[4 * j + 2] = __float_as_uint(a.z + b.z);
+      r0[4 * j + 3] = __float_as_uint(a.w + b.w);
+      const float4 a1 = *reinterpret_cast<const float4*>(mine + c * 64 + 32 + 4 * j);
+      const float4 b1 = __ldcg(reinterpret_cast<const float4*>(other + c * 64 + 32 + 4 * j));
+      r1[4 * j] = __float_as_uint(a1.x + b1.x);
+      r1[4 * j + 1] = __float_as_uint(a1.y + b1.y);
+      r1[4 * j + 2] = __float_as_uint(a1.z + b1.z);
+      r1[4 * j + 3] = __float_as_uint(a1.w + b1.w);
+    }
+    store_chunk_f16(tmOut, p, r0, r1, row0, col_base + c * 64, stg, sb, lane);
+  }
+  if (lane == 0) p.tail_cnt[slot * 8 + part] = 0;  // ready for the next launch
+}
+
 // ---------------------------------------------------------------------------------------
 // The CTA-pair kernel: 256 x 256 output tiles computed by a cluster of two CTAs with
 // tcgen05.mma.cta_group::2.  CTA r of the pair loads A rows [256m + 128r, +128) and B
@@ -1014,8 +1107,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int row0 = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;
-      epilogue_tile<Cfg::kBN, OUT_F32>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, w.split, stg,
-                                       sb, mapa_shared(smem_u32(&tempty[buf]), 0), true, lane);
+      const uint32_t release_bar = mapa_shared(smem_u32(&tempty[buf]), 0);
+      if (!OUT_F32 && w.tail_slot >= 0)
+        epilogue_tail<Cfg::kBN>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, w.tail_slot, w.split,
+                                static_cast<int>(rank) * 4 + q, stg, sb, release_bar, lane);
+      else
+        epilogue_tile<Cfg::kBN, OUT_F32>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, w.split, stg,
+                                         sb, release_bar, true, lane);
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();

@@ -89,6 +89,8 @@ typedef struct {
   int debug_flags;      /* TG_DEBUG_* below; 0 in normal use */
   int timeout_ms;       /* 0 (default 2000 ms), or the per-wait limit of the pipeline */
   int pair;             /* 0: choose; 1: use the two-CTA 256x256 tile; -1: never use it */
+  int tail;             /* 0: choose; 1: split the last partial wave's tiles in two K halves
+                           whenever the plan allows it; -1: never */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
@@ -111,6 +113,8 @@ typedef struct {
   int64_t workspace_bytes;     /* scratch needed per call */
   int kernels;                 /* kernel launches per call */
   int cta_pair;                /* 1: 256x256 tiles on clusters of two CTAs (tcgen05 cta_group::2) */
+  int64_t tail_tiles;          /* tiles of the last partial wave computed as two K halves (the
+                                  units count both halves); 0 when not used */
 } tg_plan;
 
 /*

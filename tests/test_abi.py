@@ -76,8 +76,8 @@ def test_plan_square_is_one_kernel_pair_tiles(lib):
     p = _plan(8192, 8192, 8192)
     assert p["cta_pair"] == 1
     assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 64)
-    assert p["split_k"] == 1 and p["kernels"] == 1 and p["workspace_bytes"] == 0
-    assert p["tiles_m"] == 32 and p["tiles_n"] == 32 and p["units"] == 1024
+    assert p["split_k"] == 1 and p["kernels"] == 1
+    assert p["tiles_m"] == 32 and p["tiles_n"] == 32 and p["units"] == 1024 + p["tail_tiles"]
     assert p["grid"] == 152 and p["grid"] % 2 == 0 and p["stages"] == 6
     q = _plan(8192, 8192, 8192, options={"pair": -1})
     assert q["cta_pair"] == 0 and (q["block_m"], q["block_n"]) == (128, 256)
@@ -159,3 +159,16 @@ def test_w4_argument_errors(lib):
     assert call((8, 10)) == binding.TG_ERR_MISALIGNED       # ldq not a multiple of 4
     assert call((1, p + 4)) == binding.TG_ERR_MISALIGNED    # Wq not 16-byte aligned
     assert call((4, 0)) == binding.TG_OK                    # M == 0
+
+
+def test_plan_tail_split(lib):
+    # 1024 pair tiles on 76 clusters leave 36 for a last wave: they run as 72 K halves
+    p = _plan(8192, 8192, 8192)
+    assert p["cta_pair"] == 1 and p["tail_tiles"] == 36 and p["units"] == 1024 + 36
+    assert p["workspace_bytes"] >= 36 * 2 * 256 * 256 * 4
+    q = _plan(8192, 8192, 8192, options={"tail": -1})
+    assert q["tail_tiles"] == 0 and q["units"] == 1024 and q["workspace_bytes"] == 0
+    # no tail split when more than half the clusters would be busy, or with split-K
+    assert _plan(300, 600, 1500, options={"pair": 1, "max_ctas": 6})["tail_tiles"] == 0
+    assert _plan(300, 600, 1500, options={"pair": 1, "max_ctas": 8})["tail_tiles"] == 2
+    assert _plan(8192, 8192, 8192, options={"split_k": 2})["tail_tiles"] == 0

@@ -86,7 +86,8 @@ def test_epilogue_combinations_default_plan(act, with_bias, with_res):
 
 
 @pytest.mark.parametrize("opts", [{"pair": 1}, {"pair": -1, "block_n": 192}, {"split_k": 3},
-                                  {"pair": 1, "split_k": 2}, {"force_workspace": 1}],
+                                  {"pair": 1, "split_k": 2}, {"force_workspace": 1},
+                                  {"pair": 1, "tail": 1, "max_ctas": 8}],
                          ids=lambda o: "-".join(f"{k}{v}" for k, v in o.items()))
 @pytest.mark.parametrize("act", ["gelu", "relu"])
 def test_epilogue_on_every_path(opts, act):

@@ -94,6 +94,7 @@ FORCED = [
     {"pair": 1}, {"pair": 1, "split_k": 3}, {"pair": 1, "max_ctas": 2},
     {"pair": 1, "max_ctas": 6, "panel_m": 1}, {"pair": 1, "force_repack": 1},
     {"pair": 1, "force_workspace": 1}, {"pair": -1},
+    {"pair": 1, "tail": 1, "max_ctas": 8}, {"pair": 1, "tail": 1, "max_ctas": 10},
 ]
 
 
@@ -109,7 +110,8 @@ def test_forced_plans_parity(opts):
 
 @pytest.mark.parametrize("opts", [None, {"split_k": 4}, {"max_ctas": 3},
                                   {"force_repack": 1, "split_k": 3}, {"pair": 1},
-                                  {"pair": 1, "split_k": 5, "max_ctas": 4}])
+                                  {"pair": 1, "split_k": 5, "max_ctas": 4},
+                                  {"pair": 1, "tail": 1, "max_ctas": 8}])
 @pytest.mark.parametrize("M,N,K", [(200, 300, 700), (129, 65, 4099)])
 def test_integer_inputs_bitwise(opts, M, N, K):
     a = inputs.tensor(M, K, 5, 0, "int")
@@ -168,7 +170,7 @@ def test_relu_of_identity_epilogue_and_determinism():
     a = inputs.tensor(M, K, 17, 0)
     b = inputs.tensor(K, N, 17, 1)
     for opts in (None, {"split_k": 5}, {"block_n": 128, "max_ctas": 7}, {"pair": 1},
-                 {"pair": 1, "split_k": 3, "max_ctas": 4}):
+                 {"pair": 1, "split_k": 3, "max_ctas": 4}, {"pair": 1, "tail": 1, "max_ctas": 6}):
         c1, _ = run_gpu(a, b, True, options=opts)
         c2, _ = run_gpu(a, b, True, options=opts)
         np.testing.assert_array_equal(c1.view(np.uint16), c2.view(np.uint16))
