@@ -89,8 +89,8 @@ typedef struct {
   int debug_flags;      /* TG_DEBUG_* below; 0 in normal use */
   int timeout_ms;       /* 0 (default 2000 ms), or the per-wait limit of the pipeline */
   int pair;             /* 0: choose; 1: use the two-CTA 256x256 tile; -1: never use it */
-  int tail;             /* 0: choose; 1: split the last partial wave's tiles in two K halves
-                           whenever the plan allows it; -1: never */
+  int tail;             /* 1: split the last partial wave's tiles in two K halves whenever the
+                           plan allows it (CTA-pair tiles, no split-K); 0 or -1: never */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no

@@ -162,13 +162,14 @@ def test_w4_argument_errors(lib):
 
 
 def test_plan_tail_split(lib):
-    # 1024 pair tiles on 76 clusters leave 36 for a last wave: they run as 72 K halves
-    p = _plan(8192, 8192, 8192)
+    # opt-in: 1024 pair tiles on 76 clusters leave 36 for a last wave, run as 72 K halves
+    assert _plan(8192, 8192, 8192)["tail_tiles"] == 0
+    p = _plan(8192, 8192, 8192, options={"tail": 1})
     assert p["cta_pair"] == 1 and p["tail_tiles"] == 36 and p["units"] == 1024 + 36
     assert p["workspace_bytes"] >= 36 * 2 * 256 * 256 * 4
     q = _plan(8192, 8192, 8192, options={"tail": -1})
     assert q["tail_tiles"] == 0 and q["units"] == 1024 and q["workspace_bytes"] == 0
     # no tail split when more than half the clusters would be busy, or with split-K
-    assert _plan(300, 600, 1500, options={"pair": 1, "max_ctas": 6})["tail_tiles"] == 0
-    assert _plan(300, 600, 1500, options={"pair": 1, "max_ctas": 8})["tail_tiles"] == 2
-    assert _plan(8192, 8192, 8192, options={"split_k": 2})["tail_tiles"] == 0
+    assert _plan(300, 600, 1500, options={"pair": 1, "tail": 1, "max_ctas": 6})["tail_tiles"] == 0
+    assert _plan(300, 600, 1500, options={"pair": 1, "tail": 1, "max_ctas": 8})["tail_tiles"] == 2
+    assert _plan(8192, 8192, 8192, options={"split_k": 2, "tail": 1})["tail_tiles"] == 0
