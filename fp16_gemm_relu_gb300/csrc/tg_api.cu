@@ -580,6 +580,52 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   return TG_OK;
 }
 
+// Library-owned streams and events of the host-buffer entry point, one set per device.
+constexpr int kMaxPanels = 8;
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, done_h2d = nullptr, done_d2h = nullptr;
+  cudaEvent_t a_ready[kMaxPanels] = {}, c_ready[kMaxPanels] = {};
+  std::mutex mu;
+};
+HostPipe g_pipes[kMaxDevices];
+
+tg_status host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  HostPipe& hp = g_pipes[dev];
+  if (!hp.ready) {
+    const unsigned ev = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.start, ev)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.done_h2d, ev)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.done_d2h, ev)) != cudaSuccess)
+      return cuda_fail(e);
+    for (int i = 0; i < kMaxPanels; ++i)
+      if ((e = cudaEventCreateWithFlags(&hp.a_ready[i], ev)) != cudaSuccess ||
+          (e = cudaEventCreateWithFlags(&hp.c_ready[i], ev)) != cudaSuccess)
+        return cuda_fail(e);
+    hp.ready = true;
+  }
+  *out = &hp;
+  return TG_OK;
+}
+
+// rows x width_bytes between pitched buffers: one linear copy when both are dense.
+cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch,
+                      int64_t width_bytes, int64_t rows, cudaMemcpyKind kind, cudaStream_t s) {
+  if (rows <= 0 || width_bytes <= 0) return cudaSuccess;
+  if (dpitch == width_bytes && spitch == width_bytes)
+    return cudaMemcpyAsync(dst, src, size_t(width_bytes * rows), kind, s);
+  return cudaMemcpy2DAsync(dst, size_t(dpitch), src, size_t(spitch), size_t(width_bytes),
+                           size_t(rows), kind, s);
+}
+
 }  // namespace
 
 namespace tg {
@@ -706,6 +752,10 @@ tg_status tg_gemm_relu_f16_host(const void* hA, const void* hB, void* hC, int64_
   if (M == 0 || N == 0) return TG_OK;
   DeviceState* ds = nullptr;
   if ((st = current_device(&ds)) != TG_OK) return st;
+  HostPipe* hp = nullptr;
+  if ((st = host_pipe(&hp)) != TG_OK) return st;
+  std::lock_guard<std::mutex> lock(hp->mu);  // the pipeline's streams and events are shared
+
   // device copies with 16-byte aligned rows, so the direct (TMA) path applies
   const int64_t lda_d = round_up(std::max<int64_t>(K, 1), 8);
   const int64_t ldb_d = round_up(N, 8);
@@ -723,21 +773,60 @@ tg_status tg_gemm_relu_f16_host(const void* hA, const void* hB, void* hC, int64_
   uint8_t* dA = buf;
   uint8_t* dB = buf + bytes_a;
   uint8_t* dC = buf + bytes_a + bytes_b;
+
+  // Row panels: B goes first on the host-to-device stream, then A panel by panel; each
+  // panel's GEMM runs on `stream` as soon as its rows have landed, and its C rows go back on
+  // the device-to-host stream as soon as it finishes, so copies in both directions overlap
+  // the GEMMs of other panels.
+  int64_t panels = std::min<int64_t>(kMaxPanels, std::max<int64_t>(1, M / 1024));
+  if (K == 0) panels = 1;
+  const int64_t rows = round_up(cdiv(M, panels), 256);
+  panels = cdiv(M, rows);
+  const tg_epilogue epi = epilogue_from_flag(epilogue_flag);
   st = TG_OK;
-  if (K > 0) {
-    if ((e = cudaMemcpy2DAsync(dA, size_t(lda_d) * 2, hA, size_t(lda) * 2, size_t(K) * 2,
-                               size_t(M), cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
-        (e = cudaMemcpy2DAsync(dB, size_t(ldb_d) * 2, hB, size_t(ldb) * 2, size_t(N) * 2,
-                               size_t(K), cudaMemcpyHostToDevice, stream)) != cudaSuccess)
-      st = cuda_fail(e);
-  }
-  if (st == TG_OK)
-    st = run_gemm(dA, dB, dC, M, N, K, lda_d, ldb_d, ldc_d, epilogue_from_flag(epilogue_flag),
-                  nullptr, stream);
-  if (st == TG_OK &&
-      (e = cudaMemcpy2DAsync(hC, size_t(ldc) * 2, dC, size_t(ldc_d) * 2, size_t(N) * 2,
-                             size_t(M), cudaMemcpyDeviceToHost, stream)) != cudaSuccess)
+  if ((e = cudaEventRecord(hp->start, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->h2d, hp->start, 0)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(hp->d2h, hp->start, 0)) != cudaSuccess)
     st = cuda_fail(e);
+  if (st == TG_OK && K > 0 &&
+      (e = copy_rows(dB, ldb_d * 2, hB, ldb * 2, N * 2, K, cudaMemcpyHostToDevice, hp->h2d)) !=
+          cudaSuccess)
+    st = cuda_fail(e);
+  for (int64_t pnl = 0; pnl < panels && st == TG_OK; ++pnl) {
+    const int64_t r0 = pnl * rows, mr = std::min(rows, M - r0);
+    const uint16_t* srcA = static_cast<const uint16_t*>(hA) + r0 * lda;
+    if (K > 0 && (e = copy_rows(dA + r0 * lda_d * 2, lda_d * 2, srcA, lda * 2, K * 2, mr,
+                                cudaMemcpyHostToDevice, hp->h2d)) != cudaSuccess) {
+      st = cuda_fail(e);
+      break;
+    }
+    if ((e = cudaEventRecord(hp->a_ready[pnl], hp->h2d)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, hp->a_ready[pnl], 0)) != cudaSuccess) {
+      st = cuda_fail(e);
+      break;
+    }
+    st = run_gemm(dA + r0 * lda_d * 2, dB, dC + r0 * ldc_d * 2, mr, N, K, lda_d, ldb_d, ldc_d,
+                  epi, nullptr, stream);
+    if (st != TG_OK) break;
+    uint16_t* dstC = static_cast<uint16_t*>(hC) + r0 * ldc;
+    if ((e = cudaEventRecord(hp->c_ready[pnl], stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->d2h, hp->c_ready[pnl], 0)) != cudaSuccess ||
+        (e = copy_rows(dstC, ldc * 2, dC + r0 * ldc_d * 2, ldc_d * 2, N * 2, mr,
+                       cudaMemcpyDeviceToHost, hp->d2h)) != cudaSuccess) {
+      st = cuda_fail(e);
+      break;
+    }
+  }
+  // whatever was queued, the side streams drain before the scratch goes back to the pool
+  if ((e = cudaEventRecord(hp->done_h2d, hp->h2d)) == cudaSuccess &&
+      (e = cudaEventRecord(hp->done_d2h, hp->d2h)) == cudaSuccess &&
+      (e = cudaStreamWaitEvent(stream, hp->done_h2d, 0)) == cudaSuccess)
+    e = cudaStreamWaitEvent(stream, hp->done_d2h, 0);
+  if (e != cudaSuccess) {
+    if (st == TG_OK) st = cuda_fail(e);
+    cudaStreamSynchronize(hp->h2d);
+    cudaStreamSynchronize(hp->d2h);
+  }
   cudaFreeAsync(buf, stream);
   if ((e = cudaStreamSynchronize(stream)) != cudaSuccess && st == TG_OK) st = cuda_fail(e);
   if (st == TG_OK) {

@@ -226,6 +226,22 @@ def test_host_buffer_entry_point():
     np.testing.assert_array_equal(out.view(np.uint16), c.view(np.uint16))
 
 
+@pytest.mark.parametrize("M,N,K", [(2500, 300, 200), (4100, 264, 1000)])
+def test_host_entry_point_multi_panel(M, N, K):
+    # several row panels (copies of A and C overlap the panel GEMMs), odd host strides,
+    # a ragged last panel
+    from fp16_gemm_relu_gb300 import gemm_relu_host
+
+    a = inputs.tensor(M, K, 33, 0)
+    b = inputs.tensor(K, N, 33, 1)
+    a_host = inputs.embed(a, K + 3)[:, :K]
+    out = np.full((M, N + 5), np.nan, np.float16)
+    gemm_relu_host(a_host, b, out=out[:, :N])
+    assert np.isnan(out[:, N:]).all()
+    assert_parity(np.ascontiguousarray(out[:, :N]).view(np.uint16), oracle_ref(a, b, True), K,
+                  True, where="host multi-panel")
+
+
 def test_torch_wrapper_and_views():
     from fp16_gemm_relu_gb300 import gemm_relu
 
