@@ -30,7 +30,7 @@ TG_DEBUG_DROP_FIRST_STAGE = 1
 class tg_options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "block_n", "split_k", "force_repack", "force_workspace", "panel_m", "max_ctas",
-        "debug_flags", "timeout_ms", "pair", "tail")]
+        "debug_flags", "timeout_ms", "pair", "tail", "swap_ab")]
 
 
 class tg_epilogue(ctypes.Structure):

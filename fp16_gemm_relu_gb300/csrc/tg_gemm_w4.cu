@@ -9,6 +9,17 @@ namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+template <int BMT>
+cudaError_t launch_w4t(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
+                       const tg::GemmParams& p, int grid, cudaStream_t stream) {
+  auto kern = tg::tg_gemm_w4t_kernel<BMT>;
+  constexpr int smem = tg::W4TCfg<BMT>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, tg::kW4TThreads, smem, stream>>>(a, q, s, p);
+  return cudaGetLastError();
+}
+
 template <int BN>
 cudaError_t launch_w4(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
                       const CUtensorMap& out, const tg::GemmParams& p, int grid,
@@ -58,7 +69,8 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256) return TG_ERR_INVALID_ARG;
-  if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0) return TG_ERR_INVALID_ARG;
+  if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0 || o.swap_ab < -1 || o.swap_ab > 1)
+    return TG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TG_OK;
   if (C == nullptr) return TG_ERR_INVALID_ARG;
   if (K == 0)  // no weights are read: the empty sum through the ordinary entry point
@@ -76,6 +88,48 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
   if (st != TG_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if (!tg::tensor_map_encoder(&enc)) return TG_ERR_CUDA;
+
+  const int grid_cap0 = o.max_ctas > 0 ? std::min(o.max_ctas, sms) : sms;
+  const bool swap = o.swap_ab > 0 || (o.swap_ab == 0 && M <= 128);
+  if (swap) {
+    // C^T = W^T A^T: 128 output columns per tile on the MMA's M side, BMT rows of A on its N side
+    const int bmt = M <= 64 ? 64 : 128;
+    const int64_t tm = cdiv(M, bmt), tn = cdiv(N, 128);
+    if (tm * tn >= (int64_t{1} << 31)) return TG_ERR_INVALID_ARG;
+    CUtensorMap ta, tq, ts;
+    if (encode(enc, &ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, uint64_t(K), uint64_t(M),
+               uint64_t(lda) * 2, tg::kBK, uint32_t(bmt), CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode(enc, &tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, uint64_t(cdiv(N, 8)), uint64_t(K),
+               uint64_t(ldq) * 4, 16, tg::kBK, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+        encode(enc, &ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N),
+               uint64_t(cdiv(K, group_size)), uint64_t(lds) * 2, 128, 1,
+               CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+      return TG_ERR_CUDA;
+    tg::GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.tiles_m = static_cast<int>(tm);
+    p.tiles_n = static_cast<int>(tn);
+    p.num_kb = static_cast<int>(cdiv(K, tg::kBK));
+    p.kb_per_split = p.num_kb;
+    p.splits = 1;
+    p.units = static_cast<int>(tm * tn);
+    p.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : 16, tm));
+    p.act = e.activation;
+    p.group_kb = group_size / tg::kBK;
+    p.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : 2000);
+    p.err = err;
+    p.c = static_cast<__half*>(C);
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.bias = static_cast<const __half*>(e.bias);
+    p.residual = static_cast<const __half*>(e.residual);
+    p.ldr = e.residual ? e.ldr : 0;
+    const int grid = static_cast<int>(std::min<int64_t>(p.units, grid_cap0));
+    const cudaError_t ce = bmt == 64 ? launch_w4t<64>(ta, tq, ts, p, grid, stream)
+                                     : launch_w4t<128>(ta, tq, ts, p, grid, stream);
+    return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
 
   const int64_t tiles_m = cdiv(M, tg::kBM);
   int bn = o.block_n;

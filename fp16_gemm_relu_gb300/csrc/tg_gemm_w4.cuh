@@ -8,12 +8,12 @@
 // the product rounded once (fp16 subtract of 1032 from the exact 1024 + q, then an fp16
 // multiply: both IEEE round-to-nearest-even).
 //
-// Warp roles (320 threads):
+// Warp roles (448 threads):
 //   warp 0     TMA: per stage the A tile, the packed Wq tile (64 rows x BN/8 words) and the
 //              group's scale row (BN fp16), all on one load_full barrier.
 //   warp 1     tcgen05.mma issuer; waits for load_full (A) and deq_full (decoded B).
 //   warps 2-5  epilogue (shared with the fp16 kernels).
-//   warps 6-9  dequantisers: read packed words and scales from shared memory, decode eight
+//   warps 6-13 dequantisers: read packed words and scales from shared memory, decode eight
 //              weights per word in registers and store them as the 128B-swizzled MN-major B
 //              tile the MMA expects; then fence.proxy.async and arrive on deq_full.
 // TMA zero fill makes the tails safe: scales past N or past the last group are 0, so those
@@ -24,8 +24,8 @@
 
 namespace tg {
 
-constexpr int kW4Threads = 320;
-constexpr int kDeqWarps = 4;
+constexpr int kDeqWarps = 8;  // two per scheduler (see kW4TDeqWarps)
+constexpr int kW4Threads = (2 + 4 + kDeqWarps) * 32;
 
 template <int BN>
 struct W4Cfg {
@@ -221,10 +221,10 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     __syncwarp();
   } else {
     // ------------------------------ dequantisers ------------------------------
-    const int dt = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 127
+    const int dt = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 32 * kDeqWarps - 1
     const int cw = dt % W;                               // packed word column
     const int row_first = dt / W;
-    constexpr int kRowStep = 128 / W;
+    constexpr int kRowStep = 32 * kDeqWarps / W;
     const int box = cw / 8, chunk = cw % 8;
     int stage = 0;
     uint32_t phase = 0;
@@ -257,6 +257,265 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           const int r = row_first + i * kRowStep;
           const uint4 v = dequant8(words[i], sp);
           *reinterpret_cast<uint4*>(bdst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&deq_full[stage]));
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
+// Swapped-operand variant for few rows of A (decode-like shapes): C^T = W^T · A^T.  The
+// decoded weight tile is the MMA's M side (128 output columns n, MN-major, decoded exactly as
+// in tg_gemm_w4_kernel with BN = 128) and the activations are the N side (BM rows m of A,
+// K-major), so an M = 64 problem wastes no MMA work.  TMEM holds C^T: lane = column n,
+// TMEM column = row m; the epilogue writes C[m][n] with plain stores, coalesced across lanes.
+// ---------------------------------------------------------------------------------------
+// Eight dequantiser warps (two per scheduler): a lone warp per scheduler spends ~2 cycles per
+// decode instruction and ~250 cycles per stage on its barrier wait, proxy fence and arrival;
+// two warps halve the words each decodes and overlap those fixed costs.
+constexpr int kW4TDeqWarps = 8;
+constexpr int kW4TThreads = (2 + kEpiWarps + kW4TDeqWarps) * 32;
+
+template <int BMT>
+struct W4TCfg {
+  static constexpr int kNTile = 128;                  // output columns per tile (MMA M)
+  static constexpr int kActStage = BMT * kBK * 2;     // activations, K-major
+  static constexpr int kDecStage = kBK * kNTile * 2;  // decoded weights, MN-major
+  static constexpr int kQStage = kBK * kNTile / 2;
+  static constexpr int kSStage = 1024;
+  static constexpr int kStageBytes = kActStage + kDecStage + kQStage + kSStage;
+  static constexpr int kTxBytes = kActStage + kQStage + kNTile * 2;
+  static constexpr int kStagesFit = (kSmemLimit - kSmemReserve) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kAccStride = BMT;              // TMEM columns per accumulator
+  static constexpr int kTmemCols = 2 * BMT < 32 ? 32 : 2 * BMT;
+  static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes;
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
+};
+
+// tmA: fp16 A {K, M} box {64, BMT} SW128 (K-major operand of the transposed product);
+// tmQ / tmS as tg_gemm_w4_kernel with BN = 128.  Tiles: p.tiles_m counts BMT-row blocks of A,
+// p.tiles_n counts 128-column blocks of C.
+template <int BMT>
+__global__ void __launch_bounds__(kW4TThreads, 1)
+    tg_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmS, const GemmParams p) {
+  using Cfg = W4TCfg<BMT>;
+  constexpr int S = Cfg::kStages;
+  constexpr int W = Cfg::kNTile / 8;  // 16 packed words per row
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sDec = smem;
+  uint8_t* sAct = sDec + S * Cfg::kDecStage;
+  uint8_t* sQ = sAct + S * Cfg::kActStage;
+  uint8_t* sS = sQ + S * Cfg::kQStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + S * Cfg::kSStage);
+  uint64_t* load_full = bars;
+  uint64_t* deq_full = bars + S;
+  uint64_t* empty = bars + 2 * S;
+  uint64_t* tfull = bars + 3 * S;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&load_full[s]), 1);
+      mbar_init(smem_u32(&deq_full[s]), kW4TDeqWarps);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmS);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit w = unit_of(p, u);
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
+            goto w4t_producer_done;
+          const uint32_t fb = smem_u32(&load_full[stage]);
+          mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+          tma_load_2d(smem_u32(sAct + stage * Cfg::kActStage), &tmA, fb, kb * kBK, w.m_blk * BMT);
+          tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
+          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * Cfg::kNTile,
+                      kb / p.group_kb);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    w4t_producer_done:
+      for (int s = 0; s < S; ++s)
+        if (armed & (1u << s)) wait_phase_drain(smem_u32(&load_full[s]), (armed_parity >> s) & 1u, p);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      // D (128 n x BMT m) += Wdec (128 n x 16 k, MN-major) * A^T (16 k x BMT m, K-major)
+      const uint32_t idesc = idesc_f16_f32(Cfg::kNTile, BMT, 1, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+        const Unit w = unit_of(p, u);
+        const int buf = t & 1;
+        const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+        if (!wait_phase(smem_u32(&tempty[buf]), use ^ 1u, abort_flag, p, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        bool ok = true;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&load_full[stage]), phase, abort_flag, p, kRoleMma) ||
+              !wait_phase(smem_u32(&deq_full[stage]), phase, abort_flag, p, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_mnmajor(smem_u32(sDec + stage * Cfg::kDecStage));
+          const uint64_t bd = desc_kmajor(smem_u32(sAct + stage * Cfg::kActStage));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16(d_tmem, ad + 128u * k, bd + 2u * k, idesc, (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          umma_commit(smem_u32(&empty[stage]));
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[buf]));
+      }
+      umma_commit(smem_u32(drain));
+      wait_phase_drain(smem_u32(drain), 0u, p);
+    }
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------ epilogue: C[m][n] from TMEM lane n, column m ------------
+    const int q = warp & 3;
+    int t = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++t) {
+      const Unit w = unit_of(p, u);
+      const int buf = t & 1;
+      const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const int n = w.n_blk * Cfg::kNTile + q * 32 + lane;
+      const int m_base = w.m_blk * BMT;
+      const bool n_ok = n < p.N;
+      const float bias = (n_ok && p.bias) ? __half2float(p.bias[n]) : 0.0f;
+      unsigned short* cp = reinterpret_cast<unsigned short*>(p.c);
+#pragma unroll 1
+      for (int c = 0; c < BMT / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld_x32(tl + c * 32, r);
+        tmem_wait_ld(r);
+        if (c == BMT / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+        }
+        if (n_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = m_base + c * 32 + j;
+            if (m < p.M) {
+              float x = activation(__uint_as_float(r[j]) + bias, p.act);
+              if (p.residual) x += __half2float(p.residual[static_cast<long long>(m) * p.ldr + n]);
+              cp[static_cast<long long>(m) * p.ldc + n] = __half_as_ushort(__float2half_rn(x));
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------ dequantisers (as tg_gemm_w4_kernel, BN = 128) ------------
+    const int dt = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 32 * kW4TDeqWarps - 1
+    const int cw = dt % W;
+    const int row_first = dt / W;
+    constexpr int kRowStep = 32 * kW4TDeqWarps / W;
+    const int box = cw / 8, chunk = cw % 8;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+      const Unit w = unit_of(p, u);
+      bool ok = true;
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        int ready = 0;
+        if (lane == 0)
+          ready = wait_phase(smem_u32(&load_full[stage]), phase, abort_flag, p, kRoleProducer);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (!ready) {
+          ok = false;
+          break;
+        }
+        const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
+        const uint32_t sp[4] = {prmt(sv.x, sv.z, 0x5410), prmt(sv.x, sv.z, 0x7632),
+                                prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
+        uint8_t* ddst = sDec + stage * Cfg::kDecStage + box * 8192;
+        constexpr int kRows = 64 / kRowStep;
+        uint32_t words[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) words[i] = qw[(row_first + i * kRowStep) * W + cw];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const int r = row_first + i * kRowStep;
+          const uint4 v = dequant8(words[i], sp);
+          *reinterpret_cast<uint4*>(ddst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
         }
         fence_async_smem();
         __syncwarp();

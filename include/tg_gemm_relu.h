@@ -91,6 +91,8 @@ typedef struct {
   int pair;             /* 0: choose; 1: use the two-CTA 256x256 tile; -1: never use it */
   int tail;             /* 1: split the last partial wave's tiles in two K halves whenever the
                            plan allows it (CTA-pair tiles, no split-K); 0 or -1: never */
+  int swap_ab;          /* int4 GEMM only: 0 choose (swapped for M <= 128), 1 compute C^T =
+                           W^T A^T with the decoded weights as the 128-row MMA side, -1 never */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no

@@ -92,6 +92,21 @@ def test_w4_epilogue_and_multitile(act):
     check(got0, a, Wq, S, N, G, act)
 
 
+@pytest.mark.parametrize("M,N,K,G", [(1, 257, 640, 128), (64, 1000, 4096, 128), (100, 300, 1030, 64),
+                                     (128, 2048, 2048, 256)])
+@pytest.mark.parametrize("act", ["none", "relu", "gelu"])
+def test_w4_swapped_kernel(M, N, K, G, act):
+    # C^T = W^T A^T with the decoded weights on the MMA's 128-row side (small M)
+    a, Wq, S = make(M, N, K, G, 11)
+    ACT = {"none": 0, "relu": 1, "gelu": 2}
+    bias = inputs.tensor(1, N, 12, 0).ravel()
+    res = inputs.tensor(M, N, 12, 1)
+    got = run_w4(a, Wq, S, N, G, act=ACT[act], bias=bias, residual=res, options={"swap_ab": 1})
+    check(got, a, Wq, S, N, G, act, bias, res)
+    got0 = run_w4(a, Wq, S, N, G, act=ACT[act], options={"swap_ab": 1, "max_ctas": 3})
+    check(got0, a, Wq, S, N, G, act)
+
+
 def test_w4_decode_shape_sampled():
     M, N, K, G = 64, 28672, 8192, 128
     a = inputs.tensor(M, K, 3, 0, "normal")
