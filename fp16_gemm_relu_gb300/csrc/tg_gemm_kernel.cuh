@@ -335,7 +335,11 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 }
 
 // 32 TMEM lanes x 32 consecutive 32-bit columns: thread l of the warp gets lane (base + l).
+// tcgen05.ld is a .sync.aligned instruction: the whole warp must execute it together, so the
+// warp is reconverged first (call sites follow lane-dependent branches such as ragged-edge
+// stores, after which independent thread scheduling does not promise reconvergence).
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  __syncwarp();
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
