@@ -5,9 +5,9 @@
 namespace tg {
 
 namespace {
-template <bool OUT_F32>
+template <bool OUT_F32, bool GENERAL>
 cudaError_t launch_one(const GemmLaunch& l) {
-  auto kern = tg_gemm_tc_kernel<192, OUT_F32>;
+  auto kern = tg_gemm_tc_kernel<192, OUT_F32, GENERAL>;
   constexpr int smem = TileCfg<192>::kSmemBytes;
   // per device and per function; cheap enough to repeat on every launch
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -18,7 +18,9 @@ cudaError_t launch_one(const GemmLaunch& l) {
 }  // namespace
 
 cudaError_t launch_gemm_bn192(const GemmLaunch& l, bool out_f32) {
-  return out_f32 ? launch_one<true>(l) : launch_one<false>(l);
+  const bool general = l.p.a_mn || l.p.b_k;
+  if (out_f32) return general ? launch_one<true, true>(l) : launch_one<true, false>(l);
+  return general ? launch_one<false, true>(l) : launch_one<false, false>(l);
 }
 
 }  // namespace tg

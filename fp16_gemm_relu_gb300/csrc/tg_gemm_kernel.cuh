@@ -679,13 +679,19 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
 // tmOut: OUT_F32 == false: fp16 C, dims {n_tma, M}, box {64, 32}, 128B swizzle (columns
 //        [n_tma, N) are written with plain stores through p.c)
 //        OUT_F32 == true:  f32 workspace, dims {N, M, splits}, box {32, 32, 1}, 128B swizzle
-template <int BN, bool OUT_F32>
+// GENERAL == false: A K-major and B MN-major fixed at compile time (p.a_mn and p.b_k must be
+// 0); the single producer and MMA threads then build descriptors and TMA boxes from constants,
+// which keeps their per-k-block instruction count inside the MMA time.  GENERAL == true reads
+// the layouts from p.a_mn and p.b_k (the transposed-operand GEMMs of the backward pass).
+template <int BN, bool OUT_F32, bool GENERAL>
 __global__ void __launch_bounds__(kThreads, 1)
     tg_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   using Cfg = TileCfg<BN>;
   constexpr int S = Cfg::kStages;
+  const int a_mn = GENERAL ? p.a_mn : 0;
+  const int b_k = GENERAL ? p.b_k : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -751,14 +757,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
             const uint32_t a_dst = smem_u32(sA + stage * Cfg::kAStage);
             const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
-            if (!p.a_mn) {
+            if (!a_mn) {
               tma_load_2d(a_dst, &tmA, fb, kb * kBK, w.m_blk * kBM);
             } else {
 #pragma unroll
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_2d(a_dst + j * 8192, &tmA, fb, w.m_blk * kBM + j * 64, kb * kBK);
             }
-            if (!p.b_k) {
+            if (!b_k) {
 #pragma unroll
               for (int j = 0; j < BN / 64; ++j)
                 tma_load_2d(b_dst + j * Cfg::kBBox, &tmB, fb, w.n_blk * BN + j * 64, kb * kBK);
@@ -782,8 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(kBM, BN, p.a_mn, !p.b_k);
-      const uint64_t a_step = desc_k_step(p.a_mn), b_step = desc_k_step(!p.b_k);
+      const uint32_t idesc = idesc_f16_f32(kBM, BN, a_mn, !b_k);
+      const uint64_t a_step = desc_k_step(a_mn), b_step = desc_k_step(!b_k);
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
@@ -801,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), p.a_mn);
-          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !p.b_k);
+          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), a_mn);
+          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !b_k);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
             umma_f16(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
@@ -942,14 +948,16 @@ struct PairCfg {
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
 };
 
-// Same maps as tg_gemm_tc_kernel; tiles_m/tiles_n in p count 256 x 256 pair tiles.
-template <bool OUT_F32>
+// Same maps and GENERAL as tg_gemm_tc_kernel; tiles_m/tiles_n in p count 256 x 256 pair tiles.
+template <bool OUT_F32, bool GENERAL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   using Cfg = PairCfg;
   constexpr int S = Cfg::kStages;
+  const int a_mn = GENERAL ? p.a_mn : 0;
+  const int b_k = GENERAL ? p.b_k : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1025,14 +1033,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const uint32_t a_dst = smem_u32(sA + stage * Cfg::kAStage);
             const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
-            if (!p.a_mn) {
+            if (!a_mn) {
               tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, arow);
             } else {
 #pragma unroll
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_2d_pair(a_dst + j * 8192, &tmA, fb, arow + j * 64, kb * kBK);
             }
-            if (!p.b_k) {
+            if (!b_k) {
 #pragma unroll
               for (int j = 0; j < Cfg::kHalfN / 64; ++j)
                 tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
@@ -1055,8 +1063,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer (leader) ------------------------------
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN, p.a_mn, !p.b_k);
-      const uint64_t a_step = desc_k_step(p.a_mn), b_step = desc_k_step(!p.b_k);
+      const uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN, a_mn, !b_k);
+      const uint64_t a_step = desc_k_step(a_mn), b_step = desc_k_step(!b_k);
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
@@ -1074,8 +1082,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), p.a_mn);
-          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !p.b_k);
+          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), a_mn);
+          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !b_k);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
             umma_f16_pair(d_tmem, ad + a_step * k, bd + b_step * k, idesc,

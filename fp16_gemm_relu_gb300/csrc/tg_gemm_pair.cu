@@ -4,9 +4,9 @@
 namespace tg {
 
 namespace {
-template <bool OUT_F32>
+template <bool OUT_F32, bool GENERAL>
 cudaError_t launch_one(const GemmLaunch& l) {
-  auto kern = tg_gemm_pair_kernel<OUT_F32>;
+  auto kern = tg_gemm_pair_kernel<OUT_F32, GENERAL>;
   constexpr int smem = PairCfg::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -17,11 +17,13 @@ cudaError_t launch_one(const GemmLaunch& l) {
 
 cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32) {
   if (l.grid <= 0 || (l.grid & 1)) return cudaErrorInvalidConfiguration;
-  return out_f32 ? launch_one<true>(l) : launch_one<false>(l);
+  const bool general = l.p.a_mn || l.p.b_k;
+  if (out_f32) return general ? launch_one<true, true>(l) : launch_one<true, false>(l);
+  return general ? launch_one<false, true>(l) : launch_one<false, false>(l);
 }
 
 cudaError_t gemm_pair_max_clusters(int* out) {
-  auto kern = tg_gemm_pair_kernel<false>;
+  auto kern = tg_gemm_pair_kernel<false, false>;
   constexpr int smem = PairCfg::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
