@@ -932,13 +932,20 @@ __device__ __forceinline__ void epilogue_tail(const CUtensorMap* tmOut, const Ge
 // leader's tmem-empty barrier.  Per SM and k-block this moves 32 KB (16 KB A + 16 KB B)
 // from L2 instead of the 48 KB of the single-CTA 128 x 256 tile, for the same MMA work.
 // ---------------------------------------------------------------------------------------
-struct PairCfg {
+// KB k-blocks of kBK per pipeline stage.  The forward instance uses KB = 2: its single
+// producer and MMA threads then pay one barrier wait, one expect_tx and one commit per 128 k
+// instead of per 64 k, which keeps both under the MMA time of a stage (measured per 64 k with
+// KB = 1: ~585 cycles in each thread against ~515 cycles of tensor work).
+template <int KB>
+struct PairCfgT {
+  static constexpr int kKB = KB;
   static constexpr int kBN = 256;                       // N of the pair tile
   static constexpr int kHalfN = 128;                    // B columns in each CTA
-  static constexpr int kAStage = kBM * kBK * 2;         // 16 KB
-  static constexpr int kBBox = kBK * 64 * 2;            // 8 KB
-  static constexpr int kBStage = kBK * kHalfN * 2;      // 16 KB
-  static constexpr int kStageBytes = kAStage + kBStage; // 32 KB per CTA
+  static constexpr int kAAtom = kBM * kBK * 2;          // 16 KB: 128 rows x 64 k, K-major
+  static constexpr int kAStage = KB * kAAtom;
+  static constexpr int kBBox = KB * kBK * 64 * 2;       // 64 columns x KB*64 k rows, MN-major
+  static constexpr int kBStage = 2 * kBBox;             // the CTA's 128 columns
+  static constexpr int kStageBytes = kAStage + kBStage; // KB x 32 KB per CTA
   static constexpr int kStagingBytes = kEpiWarps * 2 * kStagingBuf;
   static constexpr int kStagesFit = (kSmemLimit - kSmemReserve - kStagingBytes) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
@@ -947,15 +954,19 @@ struct PairCfg {
   static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes + kStagingBytes;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
 };
+using PairCfg = PairCfgT<1>;
+using PairCfgFwd = PairCfgT<2>;
 
 // Same maps and GENERAL as tg_gemm_tc_kernel; tiles_m/tiles_n in p count 256 x 256 pair tiles.
+// The forward instance (GENERAL == false) takes 128-k stages: tmB's box is {64 N, 128 K}.
 template <bool OUT_F32, bool GENERAL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  using Cfg = PairCfg;
+  using Cfg = PairCfgT<GENERAL ? 1 : 2>;
   constexpr int S = Cfg::kStages;
+  constexpr int KB = Cfg::kKB;
   const int a_mn = GENERAL ? p.a_mn : 0;
   const int b_k = GENERAL ? p.b_k : 0;
 
@@ -1018,7 +1029,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const Unit w = unit_of(p, u);
         const int arow = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM;
         const int bcol = w.n_blk * Cfg::kBN + static_cast<int>(rank) * Cfg::kHalfN;
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; kb += KB) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto pair_producer_done;
           if ((p.debug_flags & kDebugDropFirstStage) && cluster == 0 && rank == 0 && !dropped) {
@@ -1033,19 +1044,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const uint32_t a_dst = smem_u32(sA + stage * Cfg::kAStage);
             const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
-            if (!a_mn) {
+            if constexpr (KB > 1) {
+              // both k-blocks always load (a second one past the unit's range is never used
+              // by the MMA; past K it is zero fill), so the stage's byte count is fixed
+#pragma unroll
+              for (int h = 0; h < KB; ++h)
+                tma_load_2d_pair(a_dst + h * Cfg::kAAtom, &tmA, fb, (kb + h) * kBK, arow);
+#pragma unroll
+              for (int j = 0; j < Cfg::kHalfN / 64; ++j)
+                tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
+            } else if (!a_mn) {
               tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, arow);
             } else {
 #pragma unroll
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_2d_pair(a_dst + j * 8192, &tmA, fb, arow + j * 64, kb * kBK);
             }
-            if (!b_k) {
+            if constexpr (KB == 1) {
+              if (!b_k) {
 #pragma unroll
-              for (int j = 0; j < Cfg::kHalfN / 64; ++j)
-                tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
-            } else {
-              tma_load_2d_pair(b_dst, &tmB, fb, kb * kBK, bcol);
+                for (int j = 0; j < Cfg::kHalfN / 64; ++j)
+                  tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
+              } else {
+                tma_load_2d_pair(b_dst, &tmB, fb, kb * kBK, bcol);
+              }
             }
           }
           if (++stage == S) {
@@ -1076,18 +1098,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
         bool ok = true;
-        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        for (int kb = w.kb_begin; kb < w.kb_end; kb += KB) {
           if (!wait_phase(smem_u32(&full[stage]), phase, abort_flag, p, kRoleMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), a_mn);
-          const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !b_k);
+          if constexpr (KB > 1) {
+            // A: KB K-major atoms 16 KB apart; B: MN-major, 128 k rows per 64-column box
+            // (boxes kBBox apart: the descriptor's leading byte offset)
+            const uint64_t ad = desc_kmajor(smem_u32(sA + stage * Cfg::kAStage));
+            const uint64_t bd = sw128_desc(smem_u32(sB + stage * Cfg::kBStage), Cfg::kBBox, 1024);
+            const int nk = (w.kb_end - kb >= KB ? KB : w.kb_end - kb) * (kBK / kUmmaK);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_f16_pair(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
-                          (kb > w.kb_begin || k > 0) ? 1u : 0u);
+            for (int k = 0; k < KB * (kBK / kUmmaK); ++k)
+              if (k < nk)
+                umma_f16_pair(d_tmem,
+                              ad + static_cast<uint64_t>((k >> 2) * (Cfg::kAAtom >> 4) + 2 * (k & 3)),
+                              bd + static_cast<uint64_t>(128 * k), idesc,
+                              (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          } else {
+            const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), a_mn);
+            const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !b_k);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              umma_f16_pair(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
+                            (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          }
           umma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
           if (++stage == S) {
             stage = 0;

@@ -7,7 +7,7 @@ namespace {
 template <bool OUT_F32, bool GENERAL>
 cudaError_t launch_one(const GemmLaunch& l) {
   auto kern = tg_gemm_pair_kernel<OUT_F32, GENERAL>;
-  constexpr int smem = PairCfg::kSmemBytes;
+  constexpr int smem = PairCfgT<GENERAL ? 1 : 2>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<l.grid, kThreads, smem, l.stream>>>(l.a, l.b, l.out, l.p);  // grid is a multiple of 2
@@ -24,7 +24,7 @@ cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32) {
 
 cudaError_t gemm_pair_max_clusters(int* out) {
   auto kern = tg_gemm_pair_kernel<false, false>;
-  constexpr int smem = PairCfg::kSmemBytes;
+  constexpr int smem = PairCfgFwd::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};

@@ -102,7 +102,9 @@ typedef struct {
 
 /* What a call will do; filled by tg_plan_query (host only, no device needed). */
 typedef struct {
-  int block_m, block_n, block_k, stages;
+  int block_m, block_n, block_k;  /* output tile and the k-block unit of kblocks */
+  int stages;                      /* pipeline stages; a forward CTA-pair stage holds two
+                                      k-blocks, every other stage one */
   int split_k;                 /* K splits actually used */
   int64_t kblocks;             /* ceil(K / block_k) */
   int64_t kblocks_per_split;

@@ -78,7 +78,8 @@ def test_plan_square_is_one_kernel_pair_tiles(lib):
     assert (p["block_m"], p["block_n"], p["block_k"]) == (256, 256, 64)
     assert p["split_k"] == 1 and p["kernels"] == 1
     assert p["tiles_m"] == 32 and p["tiles_n"] == 32 and p["units"] == 1024 + p["tail_tiles"]
-    assert p["grid"] == 152 and p["grid"] % 2 == 0 and p["stages"] == 6
+    # forward CTA-pair stages hold two 64-k blocks: 3 stages of 64 KB per CTA
+    assert p["grid"] == 152 and p["grid"] % 2 == 0 and p["stages"] == 3
     q = _plan(8192, 8192, 8192, options={"pair": -1})
     assert q["cta_pair"] == 0 and (q["block_m"], q["block_n"]) == (128, 256)
     assert q["units"] == 2048 and q["grid"] == 152 and q["stages"] == 4
