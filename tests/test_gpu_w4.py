@@ -93,7 +93,7 @@ def test_w4_epilogue_and_multitile(act):
 
 
 @pytest.mark.parametrize("M,N,K,G", [(1, 257, 640, 128), (64, 1000, 4096, 128), (100, 300, 1030, 64),
-                                     (128, 2048, 2048, 256)])
+                                     (128, 2048, 2048, 256), (37, 520, 1000, 192)])
 @pytest.mark.parametrize("act", ["none", "relu", "gelu"])
 def test_w4_swapped_kernel(M, N, K, G, act):
     # C^T = W^T A^T with the decoded weights on the MMA's 128-row side (small M)
@@ -117,3 +117,25 @@ def test_w4_decode_shape_sampled():
     cols = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 200)]))
     rows = np.arange(M)
     check(got[np.ix_(rows, cols)], a, Wq[:, :], S, N, G, "relu", rows=rows, cols=cols)
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
+def test_w4_swapped_small_grid_ragged_fused_epilogue(act):
+    # several tiles per CTA (2 and 3 CTAs for 6 column tiles), a ragged last tile (N = 700
+    # leaves a partial warp of columns), M = 90 under a 128-row tile, bias + residual + the
+    # activation, repeated: the epilogue of one tile overlaps the next tile's main loop
+    M, N, K, G = 90, 700, 1536, 128
+    a, Wq, S = make(M, N, K, G, 22)
+    ACT = {"relu": 1, "gelu_tanh": 3}
+    bias = inputs.tensor(1, N, 23, 0).ravel()
+    res = inputs.tensor(M, N, 23, 1)
+    first = {}
+    for rep in range(4):
+        for cap in (2, 3):
+            got = run_w4(a, Wq, S, N, G, act=ACT[act], bias=bias, residual=res,
+                         options={"swap_ab": 1, "max_ctas": cap})
+            if rep == 0:
+                check(got, a, Wq, S, N, G, act, bias, res)
+                first[cap] = got
+            else:  # the plan fixes the summation order: repeated calls are bitwise equal
+                np.testing.assert_array_equal(got, first[cap])
