@@ -303,27 +303,47 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
 // ------------------------------ auxiliary kernels ------------------------------
 
 // dst (rows x ld_dst, 16-byte aligned rows) <- src (rows x ld_src, any 2-byte alignment).
-// One thread writes 8 consecutive elements with one 16-byte store; columns in
-// [cols, round_up(cols, 8)) are zero.
+// Output chunk c of a row is elements [8c, 8c + 8); columns in [cols, round_up(cols, 8)) are
+// written as zero.  A warp copies 32 consecutive chunks of one row.  Element 0 of a row sits
+// b bytes into an aligned 16-byte block (b even, the same for every chunk of the row), so
+// chunk c lies in blocks c and c + 1 from there: a lane loads block c, loads block c + 1 only
+// when it holds one of the chunk's elements (so no load leaves a block that holds valid data),
+// and shifts the pair by b bytes in registers.
 __global__ void tg_pack_rows_kernel(const uint16_t* __restrict__ src, int64_t ld_src,
                                     uint16_t* __restrict__ dst, int64_t ld_dst, int64_t rows,
                                     int64_t cols) {
   const int64_t cpr = (cols + 7) >> 3;
-  const int64_t total = rows * cpr;
-  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = idx / cpr;
-    const int64_t c0 = (idx - r * cpr) << 3;
-    const uint16_t* s = src + r * ld_src + c0;
-    uint16_t v[8];
+  const int64_t gpr = (cpr + 31) >> 5;  // 32-chunk groups per row
+  const int64_t items = rows * gpr;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t it = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; it < items;
+       it += nwarps) {
+    const int64_t r = it / gpr;
+    const int64_t c = ((it - r * gpr) << 5) + lane;
+    if (c >= cpr) continue;
+    const uintptr_t row = reinterpret_cast<uintptr_t>(src + r * ld_src);
+    const uint32_t b = static_cast<uint32_t>(row & 15u);
+    const uint4* blk = reinterpret_cast<const uint4*>(row - b) + c;
+    const int nvalid = static_cast<int>(cols - (c << 3) < 8 ? cols - (c << 3) : 8);
+    const uint4 lo = __ldg(blk);
+    const uint4 hi = (b + 2u * static_cast<uint32_t>(nvalid - 1) >= 16u) ? __ldg(blk + 1)
+                                                                          : make_uint4(0, 0, 0, 0);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t q = b >> 2;  // whole words to skip
+    uint32_t t[7], u[5];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = (c0 + e < cols) ? __ldg(s + e) : uint16_t(0);
-    uint4 out;
-    out.x = uint32_t(v[0]) | (uint32_t(v[1]) << 16);
-    out.y = uint32_t(v[2]) | (uint32_t(v[3]) << 16);
-    out.z = uint32_t(v[4]) | (uint32_t(v[5]) << 16);
-    out.w = uint32_t(v[6]) | (uint32_t(v[7]) << 16);
-    *reinterpret_cast<uint4*>(dst + r * ld_dst + c0) = out;
+    for (int i = 0; i < 7; ++i) t[i] = (q & 1u) ? w[i + 1] : w[i];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) u[i] = (q & 2u) ? t[i + 2] : t[i];
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o[j] = (b & 2u) ? __funnelshift_r(u[j], u[j + 1], 16) : u[j];
+      if (2 * j >= nvalid) o[j] = 0u;
+      else if (2 * j + 1 >= nvalid) o[j] &= 0xFFFFu;
+    }
+    *reinterpret_cast<uint4*>(dst + r * ld_dst + (c << 3)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
