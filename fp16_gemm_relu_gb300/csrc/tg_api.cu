@@ -246,8 +246,7 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   P.cta_pair = best_pair;
   P.block_m = best_pair ? 2 * tg::kBM : tg::kBM;
   P.block_n = best_bn;
-  P.stages = best_pair ? (ta || tb ? tg::PairCfg::kStages : tg::PairCfgFwd::kStages)
-                       : tg::gemm_stages(best_bn);
+  P.stages = best_pair ? tg::PairCfgFwd::kStages : tg::gemm_stages(best_bn);
   P.kblocks_per_split = cdiv(P.kblocks, best_s);
   P.split_k = static_cast<int>(cdiv(P.kblocks, P.kblocks_per_split));
   P.tiles_m = cdiv(M, P.block_m);
@@ -527,17 +526,17 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   std::memset(&L, 0, sizeof(L));
   // A: K-major box {64 K, 128 rows} or, stored K x M, two MN-major boxes {64 M, 64 K};
   // B: MN-major boxes {64 N, 64 K} or, stored N x K, one K-major box {64 K, BN (or 128) rows}
+  // the CTA-pair kernel stages 128 k: its MN-major boxes are {64, 128 K}
+  const uint32_t mn_box_k = P.cta_pair ? uint32_t(tg::PairCfgFwd::kKB * tg::kBK) : tg::kBK;
   CUresult cr = ta ? encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(M),
-                               uint64_t(K), uint64_t(lda_e) * 2, 64, tg::kBK)
+                               uint64_t(K), uint64_t(lda_e) * 2, 64, mn_box_k)
                    : encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(K),
                                uint64_t(M), uint64_t(lda_e) * 2, tg::kBK, tg::kBM);
   if (cr == CUDA_SUCCESS)
     cr = tb ? encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(K), uint64_t(N),
                         uint64_t(ldb_e) * 2, tg::kBK, P.cta_pair ? 128u : uint32_t(P.block_n))
             : encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(N), uint64_t(K),
-                        uint64_t(ldb_e) * 2, 64,
-                        // the forward CTA-pair kernel stages 128 k: {64 N, 128 K} boxes
-                        P.cta_pair && !ta ? uint32_t(tg::PairCfgFwd::kKB * tg::kBK) : tg::kBK);
+                        uint64_t(ldb_e) * 2, 64, mn_box_k);
   float* ws = P.workspace_epilogue ? reinterpret_cast<float*>(scratch + pl.off_w) : nullptr;
   if (cr == CUDA_SUCCESS) {
     if (ws)

@@ -943,7 +943,8 @@ struct PairCfgT {
   static constexpr int kHalfN = 128;                    // B columns in each CTA
   static constexpr int kAAtom = kBM * kBK * 2;          // 16 KB: 128 rows x 64 k, K-major
   static constexpr int kAStage = KB * kAAtom;
-  static constexpr int kBBox = KB * kBK * 64 * 2;       // 64 columns x KB*64 k rows, MN-major
+  static constexpr int kMNBox = KB * kBK * 64 * 2;      // 64 rows or columns x KB*64 k, MN-major
+  static constexpr int kBBox = kMNBox;
   static constexpr int kBStage = 2 * kBBox;             // the CTA's 128 columns
   static constexpr int kStageBytes = kAStage + kBStage; // KB x 32 KB per CTA
   static constexpr int kStagingBytes = kEpiWarps * 2 * kStagingBuf;
@@ -954,21 +955,20 @@ struct PairCfgT {
   static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes + kStagingBytes;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
 };
-using PairCfg = PairCfgT<1>;
 using PairCfgFwd = PairCfgT<2>;
 
-// Same maps and GENERAL as tg_gemm_tc_kernel; tiles_m/tiles_n in p count 256 x 256 pair tiles.
-// The forward instance (GENERAL == false) takes 128-k stages: tmB's box is {64 N, 128 K}.
-template <bool OUT_F32, bool GENERAL>
+// Same maps as tg_gemm_tc_kernel, with the operand layouts fixed at compile time (A_MN: A stored
+// K x M; B_K: B stored N x K) and 128-k stages: MN-major operands come as {64, 128 K} boxes,
+// K-major ones as one {64 K, 128} box per 64-k block.  tiles_m/tiles_n in p count 256 x 256
+// pair tiles.
+template <bool OUT_F32, bool A_MN, bool B_K>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
-  using Cfg = PairCfgT<GENERAL ? 1 : 2>;
+  using Cfg = PairCfgFwd;
   constexpr int S = Cfg::kStages;
   constexpr int KB = Cfg::kKB;
-  const int a_mn = GENERAL ? p.a_mn : 0;
-  const int b_k = GENERAL ? p.b_k : 0;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1044,30 +1044,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const uint32_t a_dst = smem_u32(sA + stage * Cfg::kAStage);
             const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
-            if constexpr (KB > 1) {
-              // both k-blocks always load (a second one past the unit's range is never used
-              // by the MMA; past K it is zero fill), so the stage's byte count is fixed
+            // both k-blocks always load (a second one past the unit's range is never used by
+            // the MMA; past K it is zero fill), so the stage's byte count is fixed
+            if constexpr (!A_MN) {
 #pragma unroll
               for (int h = 0; h < KB; ++h)
                 tma_load_2d_pair(a_dst + h * Cfg::kAAtom, &tmA, fb, (kb + h) * kBK, arow);
-#pragma unroll
-              for (int j = 0; j < Cfg::kHalfN / 64; ++j)
-                tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
-            } else if (!a_mn) {
-              tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, arow);
             } else {
 #pragma unroll
               for (int j = 0; j < kBM / 64; ++j)
-                tma_load_2d_pair(a_dst + j * 8192, &tmA, fb, arow + j * 64, kb * kBK);
+                tma_load_2d_pair(a_dst + j * Cfg::kMNBox, &tmA, fb, arow + j * 64, kb * kBK);
             }
-            if constexpr (KB == 1) {
-              if (!b_k) {
+            if constexpr (!B_K) {
 #pragma unroll
-                for (int j = 0; j < Cfg::kHalfN / 64; ++j)
-                  tma_load_2d_pair(b_dst + j * Cfg::kBBox, &tmB, fb, bcol + j * 64, kb * kBK);
-              } else {
-                tma_load_2d_pair(b_dst, &tmB, fb, kb * kBK, bcol);
-              }
+              for (int j = 0; j < Cfg::kHalfN / 64; ++j)
+                tma_load_2d_pair(b_dst + j * Cfg::kMNBox, &tmB, fb, bcol + j * 64, kb * kBK);
+            } else {
+#pragma unroll
+              for (int h = 0; h < KB; ++h)
+                tma_load_2d_pair(b_dst + h * Cfg::kAAtom, &tmB, fb, (kb + h) * kBK, bcol);
             }
           }
           if (++stage == S) {
@@ -1085,8 +1080,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer (leader) ------------------------------
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN, a_mn, !b_k);
-      const uint64_t a_step = desc_k_step(a_mn), b_step = desc_k_step(!b_k);
+      constexpr uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN, A_MN, !B_K);
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
@@ -1104,26 +1098,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          if constexpr (KB > 1) {
-            // A: KB K-major atoms 16 KB apart; B: MN-major, 128 k rows per 64-column box
-            // (boxes kBBox apart: the descriptor's leading byte offset)
-            const uint64_t ad = desc_kmajor(smem_u32(sA + stage * Cfg::kAStage));
-            const uint64_t bd = sw128_desc(smem_u32(sB + stage * Cfg::kBStage), Cfg::kBBox, 1024);
-            const int nk = (w.kb_end - kb >= KB ? KB : w.kb_end - kb) * (kBK / kUmmaK);
+          // K-major operand: KB atoms kAAtom apart, 32 bytes per 16 k inside an atom;
+          // MN-major operand: 128 k rows per 64-wide box (boxes kMNBox apart: the leading byte
+          // offset), 2048 bytes per 16 k
+          const uint32_t a_addr = smem_u32(sA + stage * Cfg::kAStage);
+          const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBStage);
+          const uint64_t ad = A_MN ? sw128_desc(a_addr, Cfg::kMNBox, 1024) : desc_kmajor(a_addr);
+          const uint64_t bd = B_K ? desc_kmajor(b_addr) : sw128_desc(b_addr, Cfg::kMNBox, 1024);
+          const int nk = (w.kb_end - kb >= KB ? KB : w.kb_end - kb) * (kBK / kUmmaK);
 #pragma unroll
-            for (int k = 0; k < KB * (kBK / kUmmaK); ++k)
-              if (k < nk)
-                umma_f16_pair(d_tmem,
-                              ad + static_cast<uint64_t>((k >> 2) * (Cfg::kAAtom >> 4) + 2 * (k & 3)),
-                              bd + static_cast<uint64_t>(128 * k), idesc,
-                              (kb > w.kb_begin || k > 0) ? 1u : 0u);
-          } else {
-            const uint64_t ad = desc_operand(smem_u32(sA + stage * Cfg::kAStage), a_mn);
-            const uint64_t bd = desc_operand(smem_u32(sB + stage * Cfg::kBStage), !b_k);
-#pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k)
-              umma_f16_pair(d_tmem, ad + a_step * k, bd + b_step * k, idesc,
-                            (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          for (int k = 0; k < KB * (kBK / kUmmaK); ++k) {
+            const uint64_t koff_k = static_cast<uint64_t>((k >> 2) * (Cfg::kAAtom >> 4) + 2 * (k & 3));
+            const uint64_t koff_mn = static_cast<uint64_t>(128 * k);
+            if (k < nk)
+              umma_f16_pair(d_tmem, ad + (A_MN ? koff_mn : koff_k), bd + (B_K ? koff_k : koff_mn),
+                            idesc, (kb > w.kb_begin || k > 0) ? 1u : 0u);
           }
           umma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
           if (++stage == S) {

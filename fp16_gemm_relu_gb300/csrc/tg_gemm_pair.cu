@@ -4,26 +4,30 @@
 namespace tg {
 
 namespace {
-template <bool OUT_F32, bool GENERAL>
+template <bool OUT_F32, bool A_MN, bool B_K>
 cudaError_t launch_one(const GemmLaunch& l) {
-  auto kern = tg_gemm_pair_kernel<OUT_F32, GENERAL>;
-  constexpr int smem = PairCfgT<GENERAL ? 1 : 2>::kSmemBytes;
+  auto kern = tg_gemm_pair_kernel<OUT_F32, A_MN, B_K>;
+  constexpr int smem = PairCfgFwd::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<l.grid, kThreads, smem, l.stream>>>(l.a, l.b, l.out, l.p);  // grid is a multiple of 2
   return cudaGetLastError();
 }
+
+template <bool OUT_F32>
+cudaError_t launch_layout(const GemmLaunch& l) {
+  if (l.p.a_mn) return l.p.b_k ? launch_one<OUT_F32, true, true>(l) : launch_one<OUT_F32, true, false>(l);
+  return l.p.b_k ? launch_one<OUT_F32, false, true>(l) : launch_one<OUT_F32, false, false>(l);
+}
 }  // namespace
 
 cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32) {
   if (l.grid <= 0 || (l.grid & 1)) return cudaErrorInvalidConfiguration;
-  const bool general = l.p.a_mn || l.p.b_k;
-  if (out_f32) return general ? launch_one<true, true>(l) : launch_one<true, false>(l);
-  return general ? launch_one<false, true>(l) : launch_one<false, false>(l);
+  return out_f32 ? launch_layout<true>(l) : launch_layout<false>(l);
 }
 
 cudaError_t gemm_pair_max_clusters(int* out) {
-  auto kern = tg_gemm_pair_kernel<false, false>;
+  auto kern = tg_gemm_pair_kernel<false, false, false>;
   constexpr int smem = PairCfgFwd::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
