@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       uint32_t armed = 0, armed_parity = 0;
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
+        // scale row of k-block kb: g = kb / group_kb, advanced with a counter (one division
+        // per tile instead of one per stage on the single producer thread)
+        int g = w.kb_begin / p.group_kb;
+        int g_rem = w.kb_begin - g * p.group_kb;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto w4_producer_done;
@@ -143,8 +147,11 @@ __global__ void __launch_bounds__(kW4Threads, 1)
           mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
           tma_load_2d(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, w.m_blk * kBM);
           tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
-          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * BN,
-                      kb / p.group_kb);
+          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * BN, g);
+          if (++g_rem == p.group_kb) {
+            g_rem = 0;
+            ++g;
+          }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -377,6 +384,10 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
       uint32_t armed = 0, armed_parity = 0;
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
+        // scale row of k-block kb: g = kb / group_kb, advanced with a counter (one division
+        // per tile instead of one per stage on the single producer thread)
+        int g = w.kb_begin / p.group_kb;
+        int g_rem = w.kb_begin - g * p.group_kb;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto w4t_producer_done;
@@ -384,8 +395,11 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
           tma_load_2d(smem_u32(sAct + stage * Cfg::kActStage), &tmA, fb, kb * kBK, w.m_blk * BMT);
           tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
-          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * Cfg::kNTile,
-                      kb / p.group_kb);
+          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * Cfg::kNTile, g);
+          if (++g_rem == p.group_kb) {
+            g_rem = 0;
+            ++g;
+          }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
