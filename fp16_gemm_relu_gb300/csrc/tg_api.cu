@@ -50,6 +50,7 @@ tg_status current_device(DeviceState** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED_DEVICE;
+  if ((e = tg::bind_thread_context(dev)) != cudaSuccess) return cuda_fail(e);
   std::lock_guard<std::mutex> lock(g_mutex);
   DeviceState& s = g_devices[dev];
   if (!s.ready) {
@@ -652,6 +653,18 @@ cudaError_t copy_rows(void* dst, int64_t dpitch, const void* src, int64_t spitch
 
 namespace tg {
 // Hooks for other translation units of this library (not part of the C ABI).
+// The tensor maps are encoded with the driver API, which works on the calling thread's
+// current context.  cudaGetDevice does not make one current, so a host thread whose first CUDA
+// call enters this library would have none: bind the runtime's context for the device once per
+// thread (cudaFree(nullptr) initialises it without changing the selected device).
+cudaError_t bind_thread_context(int dev) {
+  thread_local int bound = -1;
+  if (bound == dev) return cudaSuccess;
+  const cudaError_t e = cudaFree(nullptr);
+  if (e == cudaSuccess) bound = dev;
+  return e;
+}
+
 tg_status device_info(int* sm_count, unsigned int** err) {
   DeviceState* ds = nullptr;
   tg_status st = current_device(&ds);

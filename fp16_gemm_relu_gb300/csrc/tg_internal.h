@@ -32,6 +32,10 @@ cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32);
 // Clusters of two that can be resident at once on the current device.
 cudaError_t gemm_pair_max_clusters(int* out);
 
+// Makes the runtime's context for `dev` current in the calling thread (once per thread), so that
+// driver-API calls (tensor-map encoding) work from any host thread.
+cudaError_t bind_thread_context(int dev);
+
 // Current device's SM count and error word (checks the device; sets up library state).
 tg_status device_info(int* sm_count, unsigned int** err);
 

@@ -41,6 +41,7 @@ tg_status setup_current_device(StaticSetup** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED_DEVICE;
+  if (tg::bind_thread_context(dev) != cudaSuccess) return TG_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   StaticSetup& s = g_setup[dev];
   if (!s.done) {
