@@ -25,6 +25,12 @@
  *    error has launched nothing and written nothing.
  *  - Device support: compute capability 10.3 (GB300) only (TG_ERR_UNSUPPORTED_DEVICE).
  *  - Thread safety: every entry point may be called from several host threads at once.
+ *  - CUDA graphs: the asynchronous device-pointer entry points (tg_gemm_relu_f16, _ex,
+ *    tg_gemm_f16_epilogue, tg_gemm_f16_t, tg_relu_backward_f16, tg_gemm_w4a16_f16) may be
+ *    captured by stream capture once the calling thread has made one eager call on the device
+ *    (that first call sets up library state); scratch is taken stream-ordered from the
+ *    library's pool and becomes graph allocation nodes.  tg_gemm_relu_f16_host synchronises
+ *    and cannot be captured.
  */
 #ifndef TG_GEMM_RELU_H
 #define TG_GEMM_RELU_H
