@@ -431,8 +431,9 @@ def run_ours(args, wl):
                            "fp16/bf16 nominal ratio)" if roof["bound"] == "tensor"
                            else f"{peak_src} (MEASURED_PEAKS.json copy bandwidth)")
     if roof["bound"] == "tensor" and "bf16_tflops_sustained" in peaks:
-        # context only: the cuBLAS rate the driver measured in a seconds-long loop under the
-        # power cap (the bench's back-to-back steps run in the same regime)
+        # context only: the cuBLAS rate measured in a seconds-long loop under the power cap
+        # (MEASURED_PEAKS.json's sustained figure; the bench's back-to-back steps run in the
+        # same regime)
         roof["peak_sustained"] = peaks["bf16_tflops_sustained"] * FP16_OVER_BF16
         roof["frac_of_sustained"] = roof["achieved"] / roof["peak_sustained"]
     roof["kernel_ms"] = kernel_ms
