@@ -77,9 +77,20 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(workload: str, pass_: str, epilogue: str, dequant: str) -> str:
+    """Row name in profiles/traffic.txt: the workload alone for the forward relu GEMM, else
+    the workload with the variant (e.g. 'square8192/w4')."""
+    if (pass_, epilogue, dequant) == ("forward", "relu", "none"):
+        return workload
+    parts = [workload] + [v for v, d in ((pass_, "forward"), (epilogue, "relu"),
+                                         (dequant, "none")) if v != d]
+    return "/".join(parts)
+
+
 def traffic_from_profiles(workload: str):
     """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if it was
-    taken on the current kernel source (its 'source_hash' line must match)."""
+    taken on the current kernel source (its 'source_hash' line must match).  `workload` is a
+    traffic_key."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
@@ -310,7 +321,15 @@ def run_ours(args, wl):
                                                   1.0 / np.sqrt(wl.K))).to(dev)
         del B
         alg_bytes = 2 * wl.M * wl.K + wl.K * wl.N // 2 + 2 * wl.N * (-(-wl.K // G)) + 2 * wl.M * wl.N
-        plan = {**plan, "kernels": 1, "dequant": "w4 g128"}
+        # the int4 kernel the library picks for the two int4 workloads: the swapped-operand
+        # kernel for a few rows of A, 256 x 256 CTA-pair tiles for many
+        if wl.M <= 128:
+            plan = {"block_m": 64 if wl.M <= 64 else 128, "block_n": 128, "block_k": 64,
+                    "kernel": "tg_gemm_w4t_kernel (C^T = W^T A^T)"}
+        else:
+            plan = {"block_m": 256, "block_n": 256, "block_k": 64,
+                    "kernel": "tg_gemm_w4_pair_kernel"}
+        plan.update({"split_k": 1, "kernels": 1, "dequant": "w4 g128"})
 
         def step():
             st = lib.tg_gemm_w4a16_f16(A.data_ptr(), Wq.data_ptr(), Sc.data_ptr(), C.data_ptr(),
@@ -426,7 +445,9 @@ def run_ours(args, wl):
         achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_from_profiles(wl.name) if plan["kernels"] == 1 else None
+    roof["traffic"] = (traffic_from_profiles(traffic_key(wl.name, args.pass_, args.epilogue,
+                                                         args.dequant))
+                       if plan["kernels"] == 1 else None)
     roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json bf16 burst x {FP16_OVER_BF16} "
                            "fp16/bf16 nominal ratio)" if roof["bound"] == "tensor"
                            else f"{peak_src} (MEASURED_PEAKS.json copy bandwidth)")
@@ -451,7 +472,8 @@ def run_ours(args, wl):
                    "l2": "flushed between steps" if flush else
                          f"inputs ({in_bytes / 2**20:.0f} MiB) larger than L2",
                    "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
-                                                 "split_k", "units", "grid", "kernels")}},
+                                                 "split_k", "units", "grid", "kernels",
+                                                 "kernel") if k in plan}},
         "gpu_launches": args.steps * plan["kernels"],
         "roofline": roof,
         "clocks": sampler.summary(),

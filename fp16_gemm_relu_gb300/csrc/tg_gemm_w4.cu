@@ -1,5 +1,6 @@
 // tg_gemm_w4a16_f16: the int4-weight dequantising GEMM (see tg_gemm_w4.cuh for the kernel).
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 
 #include "tg_gemm_w4.cuh"
@@ -30,6 +31,63 @@ cudaError_t launch_w4(const CUtensorMap& a, const CUtensorMap& q, const CUtensor
   if (e != cudaSuccess) return e;
   kern<<<grid, tg::kW4Threads, smem, stream>>>(a, q, s, out, p);
   return cudaGetLastError();
+}
+
+int w4_pair_query_clusters();
+
+cudaError_t launch_w4_pair(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
+                           const CUtensorMap& out, const tg::GemmParams& p, int grid,
+                           cudaStream_t stream) {
+  constexpr int smem = tg::W4PairCfg::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(tg::tg_gemm_w4_pair_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  tg::tg_gemm_w4_pair_kernel<<<grid, tg::W4PairCfg::kThreads, smem, stream>>>(a, q, s, out, p);
+  return cudaGetLastError();
+}
+
+// Clusters of two that can be resident at once (0 if the query fails), queried once per device.
+int w4_pair_max_clusters() {
+  static std::atomic<int> cached[64];  // value + 1; 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c - 1;
+  }
+  const int n = w4_pair_query_clusters();
+  if (dev >= 0 && dev < 64) cached[dev].store(n + 1, std::memory_order_relaxed);
+  return n;
+}
+
+int w4_pair_query_clusters() {
+  constexpr int smem = tg::W4PairCfg::kSmemBytes;
+  if (cudaFuncSetAttribute(tg::tg_gemm_w4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(tg::W4PairCfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(tg::tg_gemm_w4_pair_kernel),
+                                     &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 CUresult encode(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, CUtensorMapDataType dt,
@@ -69,7 +127,8 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
   std::memset(&o, 0, sizeof(o));
   if (opt) o = *opt;
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256) return TG_ERR_INVALID_ARG;
-  if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0 || o.swap_ab < -1 || o.swap_ab > 1)
+  if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0 || o.swap_ab < -1 || o.swap_ab > 1 ||
+      o.pair < -1 || o.pair > 1)
     return TG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TG_OK;
   if (C == nullptr) return TG_ERR_INVALID_ARG;
@@ -128,6 +187,56 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
     const int grid = static_cast<int>(std::min<int64_t>(p.units, grid_cap0));
     const cudaError_t ce = bmt == 64 ? launch_w4t<64>(ta, tq, ts, p, grid, stream)
                                      : launch_w4t<128>(ta, tq, ts, p, grid, stream);
+    return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  }
+
+  // many rows: 256 x 256 tiles on CTA pairs, each CTA decoding half of the weight tile
+  // (an explicit block_n asks for the single-CTA kernel's tile width).  By default the pair
+  // kernel runs when its tiles occupy at least half of the clusters that fit at once: with
+  // fewer, the single-CTA kernel's smaller tiles spread the work over more SMs.
+  const bool want_pair = o.pair > 0 || (o.pair == 0 && o.block_n == 0 && M >= 256);
+  const int pair_clusters = want_pair ? w4_pair_max_clusters() : 0;
+  const int64_t pair_tiles = cdiv(M, 2 * tg::kBM) * cdiv(N, tg::W4PairCfg::kBN);
+  if (pair_clusters > 0 && (o.pair > 0 || 2 * pair_tiles >= pair_clusters)) {
+    const int64_t tm = cdiv(M, 2 * tg::kBM), tn = cdiv(N, tg::W4PairCfg::kBN);
+    if (tm * tn >= (int64_t{1} << 31)) return TG_ERR_INVALID_ARG;
+    CUtensorMap ta, tq, ts, tc;
+    if (encode(enc, &ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, uint64_t(K), uint64_t(M),
+               uint64_t(lda) * 2, tg::kBK, tg::kBM, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode(enc, &tq, CU_TENSOR_MAP_DATA_TYPE_UINT32, Wq, uint64_t(cdiv(N, 8)), uint64_t(K),
+               uint64_t(ldq) * 4, tg::W4PairCfg::kHalfN / 8, tg::kBK, CU_TENSOR_MAP_SWIZZLE_NONE) !=
+            CUDA_SUCCESS ||
+        encode(enc, &ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N),
+               uint64_t(cdiv(K, group_size)), uint64_t(lds) * 2, tg::W4PairCfg::kHalfN, 1,
+               CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+        encode(enc, &tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C,
+               uint64_t(std::max<int64_t>(N & ~int64_t{7}, 8)), uint64_t(M), uint64_t(ldc) * 2, 64,
+               32, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return TG_ERR_CUDA;
+    tg::GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.tiles_m = static_cast<int>(tm);
+    p.tiles_n = static_cast<int>(tn);
+    p.num_kb = static_cast<int>(cdiv(K, tg::kBK));
+    p.kb_per_split = p.num_kb;
+    p.splits = 1;
+    p.units = static_cast<int>(tm * tn);
+    p.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : 8, tm));
+    p.act = e.activation;
+    p.group_kb = group_size / tg::kBK;
+    p.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : 2000);
+    p.err = err;
+    p.c = static_cast<__half*>(C);
+    p.ldc = ldc;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.n_tma = static_cast<int>(N & ~int64_t{7});
+    p.bias = static_cast<const __half*>(e.bias);
+    p.residual = static_cast<const __half*>(e.residual);
+    p.ldr = e.residual ? e.ldr : 0;
+    int clusters = std::min<int64_t>(p.units, pair_clusters);
+    if (o.max_ctas > 0) clusters = std::min(clusters, std::max(1, o.max_ctas / 2));
+    const cudaError_t ce = launch_w4_pair(ta, tq, ts, tc, p, 2 * clusters, stream);
     return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
   }
 

@@ -287,6 +287,318 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 }
 
 // ---------------------------------------------------------------------------------------
+// CTA-pair variant for many rows of A: 256 x 256 output tiles on a cluster of two CTAs
+// (tcgen05 cta_group::2), as tg_gemm_pair_kernel.  CTA r holds A rows [256m + 128r, +128)
+// and decodes B columns [256n + 128r, +128) into its own shared memory; one MMA of 256 x 256
+// x 16 uses both CTAs' halves, so every decoded weight serves 256 rows of A and each CTA
+// decodes half the tile that tg_gemm_w4_kernel<256> decodes.  Per stage and CTA, shared
+// memory carries A 16 KB (TMA), the packed words 4 KB, the decoded tile 16 KB (written, then
+// read by the MMA) and A again 16 KB (read by the MMA): ~72 KB per 512 tensor cycles, against
+// ~112 KB for the single-CTA kernel.
+//
+// Barriers: full[s] (leader; both CTAs' A bytes via the pair TMA), qfull[s] (each CTA: its
+// packed words and scales), deq_full[s] (leader; its own dequantiser warps plus one arrival
+// forwarded from the follower), fdeq[s] (follower; its dequantiser warps), empty[s] (each
+// CTA; the leader's commit multicasts), tfull/tempty as tg_gemm_pair_kernel.  A remote
+// arrive with cluster-scope release costs ~1000 cycles of the arriving thread; one such
+// arrive per dequantiser warp and stage made the decode period ~1.6x longer, hence the local
+// fdeq barrier and a few forwarding threads that each carry every kForwarders-th stage.
+// ---------------------------------------------------------------------------------------
+struct W4PairCfg {
+  static constexpr int kBN = 256;                        // N of the pair tile
+  static constexpr int kHalfN = 128;                     // columns decoded by each CTA
+  static constexpr int kAStage = kBM * kBK * 2;          // 16 KB
+  static constexpr int kBStage = kBK * kHalfN * 2;       // 16 KB decoded, MN-major
+  static constexpr int kQStage = kBK * kHalfN / 2;       // 4 KB packed
+  static constexpr int kSStage = 1024;                   // one scale row (256 B), padded
+  static constexpr int kQTx = kQStage + kHalfN * 2;
+  static constexpr int kStageBytes = kAStage + kBStage + kQStage + kSStage;
+  static constexpr int kStagingBytes = kEpiWarps * 2 * kStagingBuf;
+  static constexpr int kStagesFit = (kSmemLimit - kSmemReserve - kStagingBytes) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kAccStride = 256;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes + kStagingBytes;
+  // Forwarding of the follower's dequantiser arrivals to the leader: kForwarders threads take
+  // the stages in turn (the MMA warp's lane 0 in the follower plus lane 0 of kFwdWarps extra
+  // warps), so that the ~1000-cycle latency of cluster-scope arrivals overlaps.
+  static constexpr int kFwdWarps = 2;
+  static constexpr int kForwarders = 1 + kFwdWarps;
+  static constexpr int kThreads = kW4Threads + 32 * kFwdWarps;
+  static_assert(kStages >= 2, "not enough shared memory");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
+  static_assert((5 * kStages + 5) * 8 + 8 <= kSmemReserve - 1024, "barriers exceed the reserve");
+};
+
+// tmA: fp16 A {K, M} box {64, 128} SW128; tmQ: uint32 Wq {ceil(N/8), K} box {16, 64};
+// tmS: fp16 scales {N, ceil(K/G)} box {128, 1}; tmOut: fp16 C {n_tma, M} box {64, 32} SW128.
+// p.tiles_m / p.tiles_n count 256 x 256 pair tiles; p.splits == 1; p.group_kb = G / 64.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads, 1)
+    tg_gemm_w4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmQ,
+                           const __grid_constant__ CUtensorMap tmS,
+                           const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  using Cfg = W4PairCfg;
+  constexpr int S = Cfg::kStages;
+  constexpr int W = Cfg::kHalfN / 8;  // packed words per row of a CTA's columns
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * Cfg::kAStage;
+  uint8_t* sQ = sB + S * Cfg::kBStage;
+  uint8_t* sS = sQ + S * Cfg::kQStage;
+  uint8_t* sStg = sS + S * Cfg::kSStage;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + Cfg::kStagingBytes);
+  uint64_t* full = bars;          // leader
+  uint64_t* qfull = bars + S;     // each CTA
+  uint64_t* deq_full = bars + 2 * S;  // leader
+  uint64_t* empty = bars + 3 * S; // each CTA
+  uint64_t* tfull = bars + 4 * S;
+  uint64_t* tempty = tfull + 2;   // leader
+  uint64_t* drain = tempty + 2;
+  uint64_t* fdeq = drain + 1;     // follower
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fdeq + S);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&qfull[s]), 1);
+      mbar_init(smem_u32(&deq_full[s]), kDeqWarps + 1);
+      mbar_init(smem_u32(&fdeq[s]), kDeqWarps);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 2 * kEpiWarps);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmQ);
+    prefetch_tmap(&tmS);
+    prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  // Follower only: forwarder f carries stages f, f + kForwarders, ... of the CTA's sequence.
+  auto forward = [&](int f) {
+    const uint32_t deq0_leader = mapa_shared(smem_u32(&deq_full[0]), 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    int seq = 0;
+    for (int u = cluster; u < p.units; u += nclusters) {
+      const Unit w = unit_of(p, u);
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++seq) {
+        if (seq % Cfg::kForwarders == f) {
+          if (!wait_phase(smem_u32(&fdeq[stage]), phase, abort_flag, p, kRoleProducer)) return;
+          mbar_arrive_cluster(deq0_leader + 8u * stage);
+        }
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  };
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer (both CTAs) ------------------------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_parity = 0;      // the leader's full barriers
+      uint32_t qarmed = 0, qarmed_parity = 0;    // this CTA's qfull barriers
+      const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
+      for (int u = cluster; u < p.units; u += nclusters) {
+        const Unit w = unit_of(p, u);
+        const int arow = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM;
+        const int bcol = w.n_blk * Cfg::kBN + static_cast<int>(rank) * Cfg::kHalfN;
+        int g = w.kb_begin / p.group_kb;
+        int g_rem = w.kb_begin - g * p.group_kb;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
+            goto w4pair_producer_done;
+          if (rank == 0) {
+            mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * Cfg::kAStage);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          tma_load_2d_pair(smem_u32(sA + stage * Cfg::kAStage), &tmA, full0_leader + 8u * stage,
+                           kb * kBK, arow);
+          const uint32_t qb = smem_u32(&qfull[stage]);
+          mbar_arrive_expect_tx(qb, Cfg::kQTx);
+          tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, qb, bcol / 8, kb * kBK);
+          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, qb, bcol, g);
+          qarmed |= 1u << stage;
+          qarmed_parity = (qarmed_parity & ~(1u << stage)) | (phase << stage);
+          if (++g_rem == p.group_kb) {
+            g_rem = 0;
+            ++g;
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    w4pair_producer_done:
+      for (int s = 0; s < S; ++s) {
+        if (armed & (1u << s)) wait_phase_drain(smem_u32(&full[s]), (armed_parity >> s) & 1u, p);
+        if (qarmed & (1u << s)) wait_phase_drain(smem_u32(&qfull[s]), (qarmed_parity >> s) & 1u, p);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer (leader) ------------------------------
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_f16_f32(2 * kBM, Cfg::kBN, 0, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      int t = 0;
+      for (int u = cluster; u < p.units; u += nclusters, ++t) {
+        const Unit w = unit_of(p, u);
+        const int buf = t & 1;
+        const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+        if (!wait_phase(smem_u32(&tempty[buf]), use ^ 1u, abort_flag, p, kRoleMma)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        bool ok = true;
+        for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (!wait_phase(smem_u32(&full[stage]), phase, abort_flag, p, kRoleMma) ||
+              !wait_phase(smem_u32(&deq_full[stage]), phase, abort_flag, p, kRoleMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_kmajor(smem_u32(sA + stage * Cfg::kAStage));
+          const uint64_t bd = desc_mnmajor(smem_u32(sB + stage * Cfg::kBStage));
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_f16_pair(d_tmem, ad + 2u * k, bd + 128u * k, idesc,
+                          (kb > w.kb_begin || k > 0) ? 1u : 0u);
+          umma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(smem_u32(&tfull[buf]), 0x3);
+      }
+      umma_commit_pair(smem_u32(drain));
+      wait_phase_drain(smem_u32(drain), 0u, p);
+    } else if (lane == 0 && rank == 1) {
+      forward(0);
+    }
+  } else if (warp >= 2 + kEpiWarps + kDeqWarps) {
+    // ------------------------------ forwarders (follower) ------------------------------
+    if (lane == 0 && rank == 1) forward(warp - (2 + kEpiWarps + kDeqWarps) + 1);
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------ epilogue (both CTAs) ------------------------------
+    const int q = warp & 3;
+    const int ew = warp - 2;
+    uint8_t* stg = sStg + ew * 2 * kStagingBuf;
+    int sb = 0;
+    int t = 0;
+    for (int u = cluster; u < p.units; u += nclusters, ++t) {
+      const Unit w = unit_of(p, u);
+      const int buf = t & 1;
+      const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
+      int ok = 0;
+      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * Cfg::kAccStride);
+      const int row0 = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;
+      const uint32_t release_bar = mapa_shared(smem_u32(&tempty[buf]), 0);
+      epilogue_tile<Cfg::kBN, false>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, 0, stg, sb,
+                                     release_bar, true, lane);
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  } else {
+    // ------------------------------ dequantisers (both CTAs) ------------------------------
+    const int dt = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 32 * kDeqWarps - 1
+    const int cw = dt % W;                               // packed word column
+    const int row_first = dt / W;
+    constexpr int kRowStep = 32 * kDeqWarps / W;
+    const int box = cw / 8, chunk = cw % 8;
+    uint64_t* deq_done = rank == 0 ? deq_full : fdeq;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = cluster; u < p.units; u += nclusters) {
+      const Unit w = unit_of(p, u);
+      bool ok = true;
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+        int ready = 0;
+        if (lane == 0)
+          ready = wait_phase(smem_u32(&qfull[stage]), phase, abort_flag, p, kRoleProducer);
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (!ready) {
+          ok = false;
+          break;
+        }
+        const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
+        const uint32_t sp[4] = {prmt(sv.x, sv.z, 0x5410), prmt(sv.x, sv.z, 0x7632),
+                                prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
+        const uint32_t* qw = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
+        uint8_t* bdst = sB + stage * Cfg::kBStage + box * 8192;
+        constexpr int kRows = 64 / kRowStep;
+        uint32_t words[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) words[i] = qw[(row_first + i * kRowStep) * W + cw];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          const int r = row_first + i * kRowStep;
+          const uint4 v = dequant8(words[i], sp);
+          *reinterpret_cast<uint4*>(bdst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&deq_done[stage]));
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+  }
+
+  // After an abort the follower cannot observe its A loads (they complete on the leader's
+  // barriers): give any that are still in flight time to land before the CTA can exit.
+  if (rank != 0 && *abort_flag && threadIdx.x == 0) __nanosleep(200000);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // all MMAs into either CTA's TMEM and all remote arrivals are done
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // Swapped-operand variant for few rows of A (decode-like shapes): C^T = W^T · A^T.  The
 // decoded weight tile is the MMA's M side (128 output columns n, MN-major, decoded exactly as
 // in tg_gemm_w4_kernel with BN = 128) and the activations are the N side (BM rows m of A,

@@ -178,9 +178,14 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
  * scales: device fp16, ceil(K/G) rows of lds values (lds >= N, multiple of 8, 16-byte
  *     aligned).  group_size G: a multiple of 64.
  * C: device fp16 M x N, 16-byte aligned, ldc a multiple of 8.  epi as tg_gemm_f16_epilogue.
- * The weights are decoded inside the GEMM kernel (never written to memory).  opt may set
- * block_n (128 or 256), max_ctas, panel_m and timeout_ms.  Misaligned arguments return
- * TG_ERR_MISALIGNED; asynchronous on `stream`.
+ * The weights are decoded inside the GEMM kernel (never written to memory).  Kernels: for
+ * M <= 128 the swapped-operand kernel (C^T = W^T A^T; opt->swap_ab); otherwise, by default for
+ * M >= 256 when the 256 x 256 tiles fill at least half of the clusters of two CTAs that fit at
+ * once, 256 x 256 tiles on CTA pairs, each CTA decoding half of the weight tile (opt->pair:
+ * 1 force, -1 never); else single-CTA 128 x block_n tiles (opt->block_n 128 or 256, which
+ * also selects this kernel).  opt may also set max_ctas (a pair counts as two CTAs),
+ * panel_m and timeout_ms.  Misaligned arguments return TG_ERR_MISALIGNED; asynchronous on
+ * `stream`.
  */
 tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales, void* C,
                             int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldq,

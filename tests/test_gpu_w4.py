@@ -139,3 +139,26 @@ def test_w4_swapped_small_grid_ragged_fused_epilogue(act):
                 first[cap] = got
             else:  # the plan fixes the summation order: repeated calls are bitwise equal
                 np.testing.assert_array_equal(got, first[cap])
+
+
+@pytest.mark.parametrize("M,N,K,G", [(256, 256, 128, 64), (333, 527, 1030, 128), (700, 1000, 640, 256),
+                                     (1024, 768, 2048, 128), (300, 600, 1000, 192)])
+def test_w4_pair_kernel(M, N, K, G):
+    # 256 x 256 tiles on CTA pairs, each CTA decoding its 128 columns; ragged M / N / K
+    a, Wq, S = make(M, N, K, G, 31)
+    got = run_w4(a, Wq, S, N, G, options={"pair": 1})
+    check(got, a, Wq, S, N, G)
+    got1 = run_w4(a, Wq, S, N, G, options={"pair": 1, "max_ctas": 2})  # one cluster, all tiles
+    check(got1, a, Wq, S, N, G)
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
+def test_w4_pair_fused_epilogue(act):
+    M, N, K, G = 520, 700, 1536, 128
+    a, Wq, S = make(M, N, K, G, 32)
+    ACT = {"relu": 1, "gelu_tanh": 3}
+    bias = inputs.tensor(1, N, 33, 0).ravel()
+    res = inputs.tensor(M, N, 33, 1)
+    got = run_w4(a, Wq, S, N, G, act=ACT[act], bias=bias, residual=res,
+                 options={"pair": 1, "max_ctas": 4})
+    check(got, a, Wq, S, N, G, act, bias, res)

@@ -68,3 +68,23 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = argparse.Namespace(steps=3, warmup=3)
     assert bench.run_reference(args, workloads.get("square8192")) is None
     assert capsys.readouterr().out == ""
+
+
+def test_traffic_rows_are_per_variant(tmp_path, monkeypatch):
+    """A variant's run (int4 weights, another epilogue, the backward pass) never reads the DRAM
+    bytes recorded for the plain forward relu GEMM of the same workload."""
+    import bench
+
+    assert bench.traffic_key("square8192", "forward", "relu", "none") == "square8192"
+    assert bench.traffic_key("square8192", "forward", "relu", "w4") == "square8192/w4"
+    assert (bench.traffic_key("square8192", "backward", "gelu", "none")
+            == "square8192/backward/gelu")
+    (tmp_path / "profiles").mkdir()
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "traffic.txt").write_text(
+        f"# header\nsquare8192 {h} 100\nsquare8192/w4 {h} 200\nskinny {h[::-1]} 300\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    assert bench.traffic_from_profiles("square8192") == 100.0
+    assert bench.traffic_from_profiles("square8192/w4") == 200.0
+    assert bench.traffic_from_profiles("skinny") is None  # taken on another source
