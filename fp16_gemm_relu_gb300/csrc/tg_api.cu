@@ -674,6 +674,19 @@ tg_status device_info(int* sm_count, unsigned int** err) {
   return TG_OK;
 }
 
+tg_status scratch_alloc(size_t bytes, cudaStream_t stream, void** out) {
+  DeviceState* ds = nullptr;
+  tg_status st = current_device(&ds);
+  if (st != TG_OK) return st;
+  const cudaError_t e = cudaMallocFromPoolAsync(out, bytes, ds->pool, stream);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = static_cast<int>(e);
+    cudaGetLastError();
+    return TG_ERR_NO_WORKSPACE;
+  }
+  return TG_OK;
+}
+
 cudaError_t error_word_address(unsigned int** out) {
   return cudaGetSymbolAddress(reinterpret_cast<void**>(out), g_tg_error_word);
 }

@@ -56,11 +56,13 @@ struct GemmParams {
   int a_mn;            // 1: A is stored K x M (M contiguous): MN-major tiles, two 64-wide boxes
   int b_k;             // 1: B is stored N x K (K contiguous): K-major tiles, one {64, rows} box
   int group_kb;        // int4-weight kernel only: k-blocks per scale group
-  // tail split (pair kernel, fp16 output): units [0, n_full) are whole tiles; each of the
-  // remaining tiles is two units, one per K half, that meet through tail_ws / tail_cnt
+  // tail split (pair kernel with fp16 output, swapped int4 kernel): units [0, n_full) are
+  // whole tiles; each of the remaining tiles is two units, one per K half, that meet through
+  // tail_ws / tail_cnt
   int tail;
   int n_full;
-  float* tail_ws;      // [slot][half][part = rank*4 + quarter][32 rows][256] float32 partials
+  float* tail_ws;      // float32 partials; pair kernel: [slot][half][part = rank*4 + quarter]
+                       // [32 rows][256]; swapped int4 kernel: [slot][half][quarter][BMT][32]
   int* tail_cnt;       // [slot][part] arrival counters, zero before the launch
   int debug_flags;
   unsigned long long timeout_ns;

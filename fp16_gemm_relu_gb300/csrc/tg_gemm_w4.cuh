@@ -605,11 +605,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
 // K-major), so an M = 64 problem wastes no MMA work.  TMEM holds C^T: lane = column n,
 // TMEM column = row m; the epilogue writes C[m][n] with plain stores, coalesced across lanes.
 // ---------------------------------------------------------------------------------------
-// Eight dequantiser warps (two per scheduler): a lone warp per scheduler spends ~2 cycles per
-// decode instruction and ~250 cycles per stage on its barrier wait, proxy fence and arrival;
-// two warps halve the words each decodes and overlap those fixed costs.
-constexpr int kW4TDeqWarps = 8;
-constexpr int kW4TThreads = (2 + kEpiWarps + kW4TDeqWarps) * 32;
+// Per-stage costs are paid by single threads (a barrier wait, an MMA issue or a commit each
+// costs its thread ~90-170 cycles), so the work of consecutive stages is dealt to parallel
+// threads: two MMA issuers take alternate k-blocks of a unit into two TMEM accumulators that
+// the epilogue adds (accumulator 0 + accumulator 1, a fixed order), and kW4TDeqGroups groups
+// of four dequantiser warps (one warp per scheduler each) take the stages in turn.  With one
+// issuer the MMA thread was busy the whole ~1030-cycle stage; now the decode sets the pace.
+constexpr int kW4TGroupWarps = 4;
+constexpr int kW4TDeqGroups = 2;
+constexpr int kW4TDeqWarps = kW4TDeqGroups * kW4TGroupWarps;
+constexpr int kW4TMma2Warp = 2 + kEpiWarps + kW4TDeqWarps;  // second MMA issuer
+constexpr int kW4TThreads = (3 + kEpiWarps + kW4TDeqWarps) * 32;
 
 template <int BMT>
 struct W4TCfg {
@@ -623,14 +629,17 @@ struct W4TCfg {
   static constexpr int kStagesFit = (kSmemLimit - kSmemReserve) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kAccStride = BMT;              // TMEM columns per accumulator
-  static constexpr int kTmemCols = 2 * BMT < 32 ? 32 : 2 * BMT;
+  // two TMEM buffers x two accumulators (even and odd k-blocks of a unit)
+  static constexpr int kTmemCols = 4 * BMT < 32 ? 32 : 4 * BMT;
   static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
 };
 
 // tmA: fp16 A {K, M} box {64, BMT} SW128 (K-major operand of the transposed product);
 // tmQ / tmS as tg_gemm_w4_kernel with BN = 128.  Tiles: p.tiles_m counts BMT-row blocks of A,
-// p.tiles_n counts 128-column blocks of C.
+// p.tiles_n counts 128-column blocks of C.  p.splits == 1.  With p.tail, units [0, n_full)
+// are whole tiles and each later tile is two units, one per K half (see unit_of); tail_ws
+// holds 2 x 4 x 32 x BMT floats per split tile and tail_cnt 4 zeroed counters per split tile.
 template <int BMT>
 __global__ void __launch_bounds__(kW4TThreads, 1)
     tg_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -663,14 +672,14 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&load_full[s]), 1);
-      mbar_init(smem_u32(&deq_full[s]), kW4TDeqWarps);
+      mbar_init(smem_u32(&deq_full[s]), kW4TGroupWarps);  // one group of dequantisers
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tfull[b]), 2);  // both MMA issuers
       mbar_init(smem_u32(&tempty[b]), kEpiWarps);
     }
-    mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(drain), 2);
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -724,9 +733,12 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
       for (int s = 0; s < S; ++s)
         if (armed & (1u << s)) wait_phase_drain(smem_u32(&load_full[s]), (armed_parity >> s) & 1u, p);
     }
-  } else if (warp == 1) {
-    // ------------------------------ MMA issuer ------------------------------
+  } else if (warp == 1 || warp == kW4TMma2Warp) {
+    // ------------------------------ MMA issuers ------------------------------
+    // Issuer j (0: warp 1, 1: the extra warp) takes the k-blocks kb_begin + j, + j + 2, ...
+    // of each unit into accumulator j of the unit's TMEM buffer; the epilogue adds the two.
     if (lane == 0) {
+      const int j = warp == 1 ? 0 : 1;
       // D (128 n x BMT m) += Wdec (128 n x 16 k, MN-major) * A^T (16 k x BMT m, K-major)
       const uint32_t idesc = idesc_f16_f32(Cfg::kNTile, BMT, 1, 0);
       int stage = 0;
@@ -738,9 +750,17 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
         const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
         if (!wait_phase(smem_u32(&tempty[buf]), use ^ 1u, abort_flag, p, kRoleMma)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccStride);
+        const uint32_t d_tmem =
+            tmem_base + static_cast<uint32_t>((buf * 2 + j) * Cfg::kAccStride);
         bool ok = true;
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+          if (((kb - w.kb_begin) & 1) != j) {
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if (!wait_phase(smem_u32(&load_full[stage]), phase, abort_flag, p, kRoleMma) ||
               !wait_phase(smem_u32(&deq_full[stage]), phase, abort_flag, p, kRoleMma)) {
             ok = false;
@@ -751,7 +771,8 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           const uint64_t bd = desc_kmajor(smem_u32(sAct + stage * Cfg::kActStage));
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_f16(d_tmem, ad + 128u * k, bd + 2u * k, idesc, (kb > w.kb_begin || k > 0) ? 1u : 0u);
+            umma_f16(d_tmem, ad + 128u * k, bd + 2u * k, idesc,
+                     (kb - w.kb_begin > 1 || k > 0) ? 1u : 0u);
           umma_commit(smem_u32(&empty[stage]));
           if (++stage == S) {
             stage = 0;
@@ -778,48 +799,118 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(buf * Cfg::kAccStride);
+                          static_cast<uint32_t>(buf * 2 * Cfg::kAccStride);
+      const bool two = w.kb_end - w.kb_begin >= 2;  // accumulator 1 holds the odd k-blocks
+      // float32 sums of rows c*32 .. c*32 + 31: accumulator 0 + accumulator 1, in that order
+      auto load_sums = [&](int c, uint32_t (&r)[32]) {
+        tmem_ld_x32(tl + c * 32, r);
+        if (two) {
+          uint32_t r1[32];
+          tmem_ld_x32(tl + Cfg::kAccStride + c * 32, r1);
+          tmem_wait_ld(r);
+          tmem_wait_ld(r1);
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            r[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(r1[i]));
+        } else {
+          tmem_wait_ld(r);
+        }
+      };
       const int n = w.n_blk * Cfg::kNTile + q * 32 + lane;
       const int m_base = w.m_blk * BMT;
       const bool n_ok = n < p.N;
       const float bias = (n_ok && p.bias) ? __half2float(p.bias[n]) : 0.0f;
       unsigned short* cp = reinterpret_cast<unsigned short*>(p.c);
+      // rows m0 .. m0 + 31 of column n, from 32 float32 sums
+      auto store_rows = [&](const uint32_t (&r)[32], int m0) {
+        if (!n_ok) return;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int m = m0 + j;
+          if (m < p.M) {
+            float x = activation(__uint_as_float(r[j]) + bias, p.act);
+            if (p.residual) x += __half2float(p.residual[static_cast<long long>(m) * p.ldr + n]);
+            cp[static_cast<long long>(m) * p.ldc + n] = __half_as_ushort(__float2half_rn(x));
+          }
+        }
+      };
+      if (w.tail_slot < 0) {
+#pragma unroll 1
+        for (int c = 0; c < BMT / 32; ++c) {
+          uint32_t r[32];
+          load_sums(c, r);
+          if (c == BMT / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+          }
+          store_rows(r, m_base + c * 32);
+        }
+        continue;
+      }
+      // One K half of a split tile: park this half's float32 sums in tail_ws ([slot][half]
+      // [quarter][m][lane]), then count arrivals on the (slot, quarter) counter.  The warp
+      // that arrives second adds the two halves (a + b == b + a in IEEE arithmetic, so the
+      // result does not depend on which half finished last), finishes the rows and resets the
+      // counter.  No warp waits for another CTA.
+      const long long per_part = 32LL * BMT;
+      float* mine = p.tail_ws + ((static_cast<long long>(w.tail_slot) * 2 + w.split) * 4 + q) *
+                                    per_part + lane;
 #pragma unroll 1
       for (int c = 0; c < BMT / 32; ++c) {
         uint32_t r[32];
-        tmem_ld_x32(tl + c * 32, r);
-        tmem_wait_ld(r);
+        load_sums(c, r);
         if (c == BMT / 32 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
         }
-        if (n_ok) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = m_base + c * 32 + j;
-            if (m < p.M) {
-              float x = activation(__uint_as_float(r[j]) + bias, p.act);
-              if (p.residual) x += __half2float(p.residual[static_cast<long long>(m) * p.ldr + n]);
-              cp[static_cast<long long>(m) * p.ldc + n] = __half_as_ushort(__float2half_rn(x));
-            }
-          }
-        }
+        for (int j = 0; j < 32; ++j) mine[(c * 32 + j) * 32] = __uint_as_float(r[j]);
       }
+      __threadfence();
+      __syncwarp();
+      int arrived = 0;
+      if (lane == 0) arrived = atomicAdd(p.tail_cnt + w.tail_slot * 4 + q, 1);
+      arrived = __shfl_sync(0xffffffffu, arrived, 0);
+      if (arrived == 0) continue;  // the other half finishes these rows
+      __threadfence();
+      const float* other = p.tail_ws +
+                           ((static_cast<long long>(w.tail_slot) * 2 + (w.split ^ 1)) * 4 + q) *
+                               per_part + lane;
+#pragma unroll 1
+      for (int c = 0; c < BMT / 32; ++c) {
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          r[j] = __float_as_uint(mine[(c * 32 + j) * 32] + __ldcg(other + (c * 32 + j) * 32));
+        store_rows(r, m_base + c * 32);
+      }
+      if (lane == 0) p.tail_cnt[w.tail_slot * 4 + q] = 0;
     }
   } else {
     // ------------------------------ dequantisers (as tg_gemm_w4_kernel, BN = 128) ------------
-    const int dt = threadIdx.x - (2 + kEpiWarps) * 32;  // 0 .. 32 * kW4TDeqWarps - 1
+    // group grp decodes stages grp, grp + kW4TDeqGroups, ... of the CTA's k-block sequence
+    const int grp = (warp - (2 + kEpiWarps)) / kW4TGroupWarps;
+    const int dt = threadIdx.x - (2 + kEpiWarps + grp * kW4TGroupWarps) * 32;  // 0 .. 127
     const int cw = dt % W;
     const int row_first = dt / W;
-    constexpr int kRowStep = 32 * kW4TDeqWarps / W;
+    constexpr int kRowStep = 32 * kW4TGroupWarps / W;
+    int seq = 0;
     const int box = cw / 8, chunk = cw % 8;
     int stage = 0;
     uint32_t phase = 0;
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       const Unit w = unit_of(p, u);
       bool ok = true;
-      for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
+      for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++seq) {
+        if (seq % kW4TDeqGroups != grp) {
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          continue;
+        }
         int ready = 0;
         if (lane == 0)
           ready = wait_phase(smem_u32(&load_full[stage]), phase, abort_flag, p, kRoleProducer);

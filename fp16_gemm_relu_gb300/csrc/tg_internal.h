@@ -42,6 +42,10 @@ tg_status device_info(int* sm_count, unsigned int** err);
 // Address of the device error word that kernels set when a pipeline wait runs out.
 cudaError_t error_word_address(unsigned int** out);
 
+// Stream-ordered scratch of `bytes` from the library's pool on the current device; give it back
+// with cudaFreeAsync on the same stream.  TG_ERR_NO_WORKSPACE if the pool cannot supply it.
+tg_status scratch_alloc(size_t bytes, cudaStream_t stream, void** out);
+
 // cuTensorMapEncodeTiled from the driver (false if the driver does not provide it).
 bool tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn);
 

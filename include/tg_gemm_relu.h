@@ -96,7 +96,10 @@ typedef struct {
   int timeout_ms;       /* 0 (default 2000 ms), or the per-wait limit of the pipeline */
   int pair;             /* 0: choose; 1: use the two-CTA 256x256 tile; -1: never use it */
   int tail;             /* 1: split the last partial wave's tiles in two K halves whenever the
-                           plan allows it (CTA-pair tiles, no split-K); 0 or -1: never */
+                           plan allows it (CTA-pair tiles, no split-K; or the int4 GEMM's
+                           swapped kernel); -1: never; 0: never, except in the int4 GEMM's
+                           swapped kernel, which splits when the last wave holds at most half
+                           a grid of tiles */
   int swap_ab;          /* int4 GEMM only: 0 choose (swapped for M <= 128), 1 compute C^T =
                            W^T A^T with the decoded weights as the 128-row MMA side, -1 never */
 } tg_options;
@@ -183,9 +186,10 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
  * M >= 256 when the 256 x 256 tiles fill at least half of the clusters of two CTAs that fit at
  * once, 256 x 256 tiles on CTA pairs, each CTA decoding half of the weight tile (opt->pair:
  * 1 force, -1 never); else single-CTA 128 x block_n tiles (opt->block_n 128 or 256, which
- * also selects this kernel).  opt may also set max_ctas (a pair counts as two CTAs),
- * panel_m and timeout_ms.  Misaligned arguments return TG_ERR_MISALIGNED; asynchronous on
- * `stream`.
+ * also selects this kernel).  opt may also set max_ctas (a pair counts as two CTAs), tail
+ * (swapped kernel: the last partial wave's tiles as two K halves), panel_m and timeout_ms.
+ * A split tail takes stream-ordered scratch from the library's pool (TG_ERR_NO_WORKSPACE if
+ * unavailable).  Misaligned arguments return TG_ERR_MISALIGNED; asynchronous on `stream`.
  */
 tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales, void* C,
                             int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldq,

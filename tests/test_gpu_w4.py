@@ -141,6 +141,35 @@ def test_w4_swapped_small_grid_ragged_fused_epilogue(act):
                 np.testing.assert_array_equal(got, first[cap])
 
 
+@pytest.mark.parametrize("cap,tail", [(4, 1), (4, 0), (8, 0), (8, -1), (3, 1)])
+def test_w4_swapped_tail_split(cap, tail):
+    # 11 column tiles: with 4 CTAs the last wave holds 3 tiles (split only when forced), with 8
+    # CTAs it holds 3 of 8 (split by default: 6 half-tiles fit one wave), with 3 CTAs 2 of 3.
+    # K = 1030 gives 17 k-blocks: halves of 9 and 8, the second ending in a partial block and a
+    # partial scale group.  Split tiles meet through the float32 workspace; the result must
+    # match the oracle and repeat bit for bit (a + b == b + a, whichever half lands second).
+    M, N, K, G = 90, 1300, 1030, 64
+    a, Wq, S = make(M, N, K, G, 31)
+    bias = inputs.tensor(1, N, 32, 0).ravel()
+    res = inputs.tensor(M, N, 32, 1)
+    opts = {"swap_ab": 1, "max_ctas": cap, "tail": tail}
+    got = run_w4(a, Wq, S, N, G, act=3, bias=bias, residual=res, options=opts)
+    check(got, a, Wq, S, N, G, "gelu_tanh", bias, res)
+    for _ in range(3):
+        np.testing.assert_array_equal(run_w4(a, Wq, S, N, G, act=3, bias=bias, residual=res,
+                                             options=opts), got)
+    plain = run_w4(a, Wq, S, N, G, act=1, options=opts)
+    check(plain, a, Wq, S, N, G, "relu")
+
+
+def test_w4_swapped_tail_split_single_k_block():
+    # one k-block cannot be halved: the forced split falls back to whole tiles
+    M, N, K, G = 64, 1300, 64, 64
+    a, Wq, S = make(M, N, K, G, 33)
+    got = run_w4(a, Wq, S, N, G, act=1, options={"swap_ab": 1, "max_ctas": 4, "tail": 1})
+    check(got, a, Wq, S, N, G, "relu")
+
+
 @pytest.mark.parametrize("M,N,K,G", [(256, 256, 128, 64), (333, 527, 1030, 128), (700, 1000, 640, 256),
                                      (1024, 768, 2048, 128), (300, 600, 1000, 192)])
 def test_w4_pair_kernel(M, N, K, G):
