@@ -472,8 +472,8 @@ def run_ours(args, wl):
                    "l2": "flushed between steps" if flush else
                          f"inputs ({in_bytes / 2**20:.0f} MiB) larger than L2",
                    "plan": {k: plan[k] for k in ("block_m", "block_n", "block_k", "stages",
-                                                 "split_k", "units", "grid", "kernels",
-                                                 "kernel") if k in plan}},
+                                                 "split_k", "tail_tiles", "units", "grid",
+                                                 "kernels", "kernel") if k in plan}},
         "gpu_launches": args.steps * plan["kernels"],
         "roofline": roof,
         "clocks": sampler.summary(),

@@ -258,11 +258,13 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
                      : static_cast<int>(std::min<int64_t>(P.units, grid_cap));
   P.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : kDefaultPanel, P.tiles_m));
   P.workspace_epilogue = (P.split_k > 1 || !c_direct) ? 1 : 0;
-  // Tail split (opt-in, tg_options.tail = 1): when the last wave of pair tiles would leave
-  // more than half the clusters idle, its r tiles run as 2r K halves instead.  Measured on
-  // 8192^3 under the GPU's power cap it does not pay for its float32 partial traffic (idle SMs
-  // let the busy ones clock higher), so it is not chosen automatically.
-  if (P.cta_pair && P.split_k == 1 && !P.workspace_epilogue && o.tail > 0 && P.kblocks >= 2) {
+  // Tail split (tg_options.tail: 0 chooses, 1 forces, -1 never): when the last wave of pair
+  // tiles would leave more than half the clusters idle, its r tiles run as 2r K halves
+  // instead.  On 8192^3 (36 tiles left for 76 clusters) launches interleaved with whole-tile
+  // launches measured ~8 us (1.3%) faster; under the power cap the idle SMs of a partial wave
+  // let the busy ones clock higher, which is why the gain is below the 3.8% the cycle count
+  // predicts.
+  if (P.cta_pair && P.split_k == 1 && !P.workspace_epilogue && o.tail >= 0 && P.kblocks >= 2) {
     const int64_t clusters = P.grid / 2;
     const int64_t r = P.units % clusters;
     if (r > 0 && 2 * r <= clusters && P.units > clusters) {

@@ -872,9 +872,11 @@ __device__ __forceinline__ void epilogue_tail(const CUtensorMap* tmOut, const Ge
                                               uint32_t tl, int row0, int col_base, int slot,
                                               int half, int part, uint8_t* stg, int& sb,
                                               uint32_t release_bar, int lane) {
+  // [column][row] within the part: for each column the warp's 32 rows are 128 contiguous
+  // bytes, so every store and load below is one coalesced line per warp
   const long long per_part = 32LL * BN;
   float* mine = p.tail_ws + ((static_cast<long long>(slot) * 2 + half) * 8 + part) * per_part +
-                lane * BN;
+                lane;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t r[32];
@@ -885,11 +887,8 @@ __device__ __forceinline__ void epilogue_tail(const CUtensorMap* tmOut, const Ge
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(release_bar);
     }
-    float4* d = reinterpret_cast<float4*>(mine + c * 32);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      d[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                         __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    for (int j = 0; j < 32; ++j) mine[(c * 32 + j) * 32] = __uint_as_float(r[j]);
   }
   __threadfence();
   __syncwarp();
@@ -899,24 +898,15 @@ __device__ __forceinline__ void epilogue_tail(const CUtensorMap* tmOut, const Ge
   if (arrived == 0) return;  // the other half completes this block
   __threadfence();
   const float* other = p.tail_ws + ((static_cast<long long>(slot) * 2 + (half ^ 1)) * 8 + part) *
-                                       per_part + lane * BN;
+                                       per_part + lane;
 #pragma unroll 1
   for (int c = 0; c < BN / 64; ++c) {
     uint32_t r0[32], r1[32];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float4 a = *reinterpret_cast<const float4*>(mine + c * 64 + 4 * j);
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(other + c * 64 + 4 * j));
-      r0[4 * j] = __float_as_uint(a.x + b.x);
-      r0[4 * j + 1] = __float_as_uint(a.y + b.y);
-      r0[4 * j + 2] = __float_as_uint(a.z + b.z);
-      r0[4 * j + 3] = __float_as_uint(a.w + b.w);
-      const float4 a1 = *reinterpret_cast<const float4*>(mine + c * 64 + 32 + 4 * j);
-      const float4 b1 = __ldcg(reinterpret_cast<const float4*>(other + c * 64 + 32 + 4 * j));
-      r1[4 * j] = __float_as_uint(a1.x + b1.x);
-      r1[4 * j + 1] = __float_as_uint(a1.y + b1.y);
-      r1[4 * j + 2] = __float_as_uint(a1.z + b1.z);
-      r1[4 * j + 3] = __float_as_uint(a1.w + b1.w);
+    for (int j = 0; j < 32; ++j) {
+      r0[j] = __float_as_uint(mine[(c * 64 + j) * 32] + __ldcg(other + (c * 64 + j) * 32));
+      r1[j] = __float_as_uint(mine[(c * 64 + 32 + j) * 32] +
+                              __ldcg(other + (c * 64 + 32 + j) * 32));
     }
     store_chunk_f16(tmOut, p, r0, r1, row0, col_base + c * 64, stg, sb, lane);
   }

@@ -95,11 +95,12 @@ typedef struct {
   int debug_flags;      /* TG_DEBUG_* below; 0 in normal use */
   int timeout_ms;       /* 0 (default 2000 ms), or the per-wait limit of the pipeline */
   int pair;             /* 0: choose; 1: use the two-CTA 256x256 tile; -1: never use it */
-  int tail;             /* 1: split the last partial wave's tiles in two K halves whenever the
-                           plan allows it (CTA-pair tiles, no split-K; or the int4 GEMM's
-                           swapped kernel); -1: never; 0: never, except in the int4 GEMM's
-                           swapped kernel, which splits when the last wave holds at most half
-                           a grid of tiles */
+  int tail;             /* run the last partial wave's tiles as two K halves that meet through
+                           a float32 workspace.  CTA-pair plans without split-K, with 0 or 1:
+                           when at least one full wave precedes a last wave that holds at most
+                           half the clusters.  The int4 GEMM's swapped kernel: with 0 when the
+                           last wave holds at most half a grid, with 1 whenever it is partial.
+                           -1: never */
   int swap_ab;          /* int4 GEMM only: 0 choose (swapped for M <= 128), 1 compute C^T =
                            W^T A^T with the decoded weights as the 128-row MMA side, -1 never */
 } tg_options;

@@ -163,11 +163,13 @@ def test_w4_argument_errors(lib):
 
 
 def test_plan_tail_split(lib):
-    # opt-in: 1024 pair tiles on 76 clusters leave 36 for a last wave, run as 72 K halves
-    assert _plan(8192, 8192, 8192)["tail_tiles"] == 0
-    p = _plan(8192, 8192, 8192, options={"tail": 1})
+    # by default: 1024 pair tiles on 76 clusters leave 36 for a last wave, run as 72 K halves
+    p = _plan(8192, 8192, 8192)
     assert p["cta_pair"] == 1 and p["tail_tiles"] == 36 and p["units"] == 1024 + 36
     assert p["workspace_bytes"] >= 36 * 2 * 256 * 256 * 4
+    assert _plan(8192, 8192, 8192, options={"tail": 1}) == p
+    # 64 pair tiles on 76 clusters: no full wave before the last, nothing to balance
+    assert _plan(2048, 2048, 2048)["tail_tiles"] == 0
     q = _plan(8192, 8192, 8192, options={"tail": -1})
     assert q["tail_tiles"] == 0 and q["units"] == 1024 and q["workspace_bytes"] == 0
     # no tail split when more than half the clusters would be busy, or with split-K
