@@ -88,3 +88,32 @@ def test_large_workloads_integer_inputs_bitwise(name):
     rows, cols = sample_grid(wl.M, wl.N, 40, wl.seed + 100)
     ref = oracle.gemm_relu(a, b, relu=True, rows=rows, cols=cols, want=("f32",))
     np.testing.assert_array_equal(full[np.ix_(rows, cols)], ref["out16_f32acc"])
+
+
+def test_default_tail_split_with_ragged_edges():
+    # 20 x 16 = 320 pair tiles: four full waves of 76 clusters, then 16 tiles that the default
+    # plan runs as 32 K halves.  M, N and K all end in partial tiles (5000 = 19*256 + 136,
+    # 4000 = 15*256 + 160, 1000 = 15*64 + 40), so the split tiles include edge tiles and the
+    # second K half ends in a partial k-block.
+    M, N, K = 5000, 4000, 1000
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, plan = binding.tg_plan_query(0x1000, 0x2000, 0x3000, M, N, K, K, N, N, sms)
+    assert st == binding.TG_OK and plan["cta_pair"] == 1
+    clusters = plan["grid"] // 2
+    r = (plan["tiles_m"] * plan["tiles_n"]) % clusters
+    assert plan["tail_tiles"] == (r if 0 < 2 * r <= clusters else 0)
+    a = inputs.tensor(M, K, 61, 0)
+    b = inputs.tensor(K, N, 61, 1)
+    C = run_default(a, b)
+    assert torch.equal(C.view(torch.int16), run_default(a, b).view(torch.int16)), "not deterministic"
+    full = C.cpu().numpy().view(np.uint16)
+    # rows and columns of the last tile row/column (where the split tiles sit) plus a sample
+    rows = np.unique(np.concatenate([np.arange(4864, M, 7), sample_grid(M, N, 30, 62)[0]]))
+    cols = np.unique(np.concatenate([np.arange(3840, N, 5), sample_grid(M, N, 30, 63)[1]]))
+    ref = oracle.gemm_relu(a, b, relu=True, rows=rows, cols=cols)
+    assert_parity(full[np.ix_(rows, cols)], ref, K, True, where="tail split, ragged")
+    ai = inputs.tensor(M, K, 64, 0, "int")
+    bi = inputs.tensor(K, N, 64, 1, "int")
+    fi = run_default(ai, bi).cpu().numpy().view(np.uint16)
+    refi = oracle.gemm_relu(ai, bi, relu=True, rows=rows, cols=cols, want=("f32",))
+    np.testing.assert_array_equal(fi[np.ix_(rows, cols)], refi["out16_f32acc"])
