@@ -324,7 +324,13 @@ def run_ours(args, wl):
         # the int4 kernel the library picks for the two int4 workloads: the swapped-operand
         # kernel for a few rows of A, 256 x 256 CTA-pair tiles for many
         if wl.M <= 128:
-            plan = {"block_m": 64 if wl.M <= 64 else 128, "block_n": 128, "block_k": 64,
+            # the library's rule for the swapped kernel: a last wave of at most half a grid
+            # of tiles runs as two K halves
+            bmt = 64 if wl.M <= 64 else 128
+            tiles = -(-wl.M // bmt) * -(-wl.N // 128)
+            r = tiles % props.multi_processor_count
+            tail = r if (-(-wl.K // 64) >= 2 and 0 < 2 * r <= props.multi_processor_count) else 0
+            plan = {"block_m": bmt, "block_n": 128, "block_k": 64, "tail_tiles": tail,
                     "kernel": "tg_gemm_w4t_kernel (C^T = W^T A^T)"}
         else:
             plan = {"block_m": 256, "block_n": 256, "block_k": 64,
