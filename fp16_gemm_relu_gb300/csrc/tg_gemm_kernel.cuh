@@ -621,7 +621,21 @@ __device__ __forceinline__ void store_chunk_f16(const CUtensorMap* tmOut, const 
 // TMA store.  After the last tcgen05.ld the warp releases the accumulator by arriving on
 // `release_bar` (a CTA-local barrier, or with `remote` a shared::cluster address of the
 // barrier in another CTA of the cluster).
-template <int BN, bool OUT_F32>
+// Within each group of 8 columns, a tile whose B columns were stored in the order
+// 0,4,1,5,2,6,3,7 (PERM8) holds output column q at position 2 (q mod 4) + q div 4; this puts
+// 32 such columns back in output order (a register reorder, no instructions).
+__device__ __forceinline__ void unperm8(uint32_t (&r)[32]) {
+  uint32_t t[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) t[i] = r[i];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) r[8 * g + q] = t[8 * g + ((q & 3) << 1) + (q >> 2)];
+  }
+}
+
+template <int BN, bool OUT_F32, bool PERM8 = false>
 __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const GemmParams& p,
                                               uint32_t tl, int row0, int col_base, int split,
                                               uint8_t* stg, int& sb, uint32_t release_bar,
@@ -645,6 +659,10 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
       tmem_ld_x32(tl + c * 64 + 32, r1);
       tmem_wait_ld(r1);
       if (c == BN / 64 - 1) release();
+      if constexpr (PERM8) {
+        unperm8(r0);
+        unperm8(r1);
+      }
       store_chunk_f16(tmOut, p, r0, r1, row0, col_base + c * 64, stg, sb, lane);
     }
   } else {

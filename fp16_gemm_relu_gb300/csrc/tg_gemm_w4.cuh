@@ -50,7 +50,10 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 }
 
 // Eight weights of one packed word; sp[e] holds the scales of columns (e, e+4).  Returns the
-// fp16 weights of columns 0..7 in order, two per 32-bit word.
+// fp16 weights in the column order 0,4,1,5,2,6,3,7, two per 32-bit word: the order in which
+// the nibble pairs come out.  The kernels store the decoded tile in that order and undo it in
+// their epilogues (a register reorder, or the lane's output column), which saves the four
+// byte permutes per word that column order would cost.
 __device__ __forceinline__ uint4 dequant8(uint32_t w, const uint32_t (&sp)[4]) {
   const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
   uint32_t pr[4];
@@ -61,8 +64,12 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, const uint32_t (&sp)[4]) {
     h = __hmul2(h, *reinterpret_cast<const __half2*>(&sp[e]));        // one rounding
     pr[e] = *reinterpret_cast<uint32_t*>(&h);                          // columns (e, e+4)
   }
-  return make_uint4(prmt(pr[0], pr[1], 0x5410), prmt(pr[2], pr[3], 0x5410),
-                    prmt(pr[0], pr[1], 0x7632), prmt(pr[2], pr[3], 0x7632));
+  return make_uint4(pr[0], pr[1], pr[2], pr[3]);
+}
+
+// Output column held at position l of a decoded tile (see dequant8).
+__device__ __forceinline__ int perm8_column(int l) {
+  return (l & ~7) + ((l & 1) << 2) + ((l & 7) >> 1);
 }
 
 // tmA: fp16 A {K, M} box {64, 128} SW128; tmQ: uint32 Wq {ceil(N/8), K} box {BN/8, 64};
@@ -221,8 +228,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * Cfg::kAccStride);
-      epilogue_tile<BN, false>(&tmOut, p, tl, w.m_blk * kBM + q * 32, w.n_blk * BN, 0, stg, sb,
-                               smem_u32(&tempty[buf]), false, lane);
+      epilogue_tile<BN, false, true>(&tmOut, p, tl, w.m_blk * kBM + q * 32, w.n_blk * BN, 0,
+                                     stg, sb, smem_u32(&tempty[buf]), false, lane);
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
@@ -531,8 +538,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
                           static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int row0 = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;
       const uint32_t release_bar = mapa_shared(smem_u32(&tempty[buf]), 0);
-      epilogue_tile<Cfg::kBN, false>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, 0, stg, sb,
-                                     release_bar, true, lane);
+      epilogue_tile<Cfg::kBN, false, true>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, 0, stg,
+                                           sb, release_bar, true, lane);
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
@@ -816,7 +823,7 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           tmem_wait_ld(r);
         }
       };
-      const int n = w.n_blk * Cfg::kNTile + q * 32 + lane;
+      const int n = w.n_blk * Cfg::kNTile + perm8_column(q * 32 + lane);  // TMEM lane -> column
       const int m_base = w.m_blk * BMT;
       const bool n_ok = n < p.N;
       const float bias = (n_ok && p.bias) ? __half2float(p.bias[n]) : 0.0f;
