@@ -479,6 +479,29 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   }
 }
 
+// Bounded wait for roles that wait long and gain nothing from waking early (an epilogue
+// waiting for a whole tile's main loop): sleeps between polls so that the waiting warp does
+// not take issue slots from the warps doing the stage work.
+__device__ __forceinline__ bool wait_phase_sleepy(uint32_t bar, uint32_t parity,
+                                                  volatile uint32_t* abort_flag,
+                                                  const GemmParams& p, uint32_t role) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > p.timeout_ns) {
+        *abort_flag = 1u;
+        __threadfence_block();
+        atomicOr(p.err, 1u | (role << 8));
+        return false;
+      }
+    }
+  }
+}
+
 // Bounded wait that ignores the abort flag: used while draining work already in flight.
 __device__ __forceinline__ bool wait_phase_drain(uint32_t bar, uint32_t parity,
                                                  const GemmParams& p) {

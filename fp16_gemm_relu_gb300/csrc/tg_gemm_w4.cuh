@@ -222,7 +222,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       const int buf = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
       int ok = 0;
-      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      if (lane == 0)
+        ok = wait_phase_sleepy(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -530,7 +531,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
       const int buf = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
       int ok = 0;
-      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      if (lane == 0)
+        ok = wait_phase_sleepy(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -801,7 +803,8 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
       const int buf = t & 1;
       const uint32_t use = static_cast<uint32_t>(t >> 1) & 1u;
       int ok = 0;
-      if (lane == 0) ok = wait_phase(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
+      if (lane == 0)
+        ok = wait_phase_sleepy(smem_u32(&tfull[buf]), use, abort_flag, p, kRoleEpilogue);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
