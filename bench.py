@@ -224,16 +224,23 @@ def whole_job_tflops(world: int, steps: int, flops_per_step: float, total_ms: fl
     return world * steps * flops_per_step / (total_ms * 1e-3) / 1e12
 
 
+def sample_rows(wl, a, b, target_s: float, relu=True) -> int:
+    """Rows of C that one oracle call computes in about target_s seconds: each call has a
+    fixed cost (decoding B) plus a cost per row of C, calibrated on two small calls."""
+    import oracle
+
+    t1, _, _ = oracle.timed_rows(a, b, 8, relu=relu)
+    t2, _, _ = oracle.timed_rows(a, b, 40, relu=relu)
+    per_row = max((t2 - t1) / 32, 1e-6)
+    fixed = max(t1 - 8 * per_row, 0.0)
+    return int(max(1, min(wl.M, 0.9 * (target_s - fixed) / per_row)))
+
+
 def cpu_baseline(wl, a, b, target_s: float, relu=True):
     """The oracle as it stands, on a bounded sample: the first R rows of C."""
     import oracle
 
-    # calibrate: each call has a fixed cost (decoding B) plus a cost per row of C
-    t1, _, _ = oracle.timed_rows(a, b, 4, relu=relu)
-    t2, _, _ = oracle.timed_rows(a, b, 12, relu=relu)
-    per_row = max((t2 - t1) / 8, 1e-6)
-    fixed = max(t1 - 4 * per_row, 0.0)
-    rows = int(max(1, min(wl.M, (target_s - fixed) / per_row)))
+    rows = sample_rows(wl, a, b, target_s, relu)
     dt, flops, threads = oracle.timed_rows(a, b, rows, relu=relu)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"first {rows} of {wl.M} rows of C ({rows}x{wl.N}x{wl.K}), float32 "
@@ -249,11 +256,10 @@ def run_reference(args, wl):
 
     a, b = wl.make_a(), wl.make_b()
     steps, warm = max(args.steps, 1), max(args.warmup, 0)
-    budget = 150.0 / (steps + warm)  # the whole run within a few minutes
-    dt, _, _ = oracle.timed_rows(a, b, 1)
-    rows = int(max(1, min(wl.M, budget / max(dt, 1e-6))))
-    for _ in range(warm):
-        oracle.timed_rows(a, b, rows)
+    budget = 150.0 / steps  # the timed steps within a few minutes
+    rows = sample_rows(wl, a, b, budget)
+    for _ in range(warm):  # warm caches and threads on a shorter sample
+        oracle.timed_rows(a, b, min(rows, 64))
     times = []
     flops = 0.0
     threads = oracle.max_threads()
