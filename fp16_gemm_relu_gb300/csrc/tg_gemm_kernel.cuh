@@ -673,6 +673,10 @@ __device__ __forceinline__ void epilogue_tile(const CUtensorMap* tmOut, const Ge
         mbar_arrive(release_bar);
     }
   };
+  if (row0 >= p.M) {  // none of this warp's 32 rows is in C (e.g. M = 64 under a 128-row tile)
+    release();
+    return;
+  }
   if constexpr (!OUT_F32) {
 #pragma unroll 1
     for (int c = 0; c < BN / 64; ++c) {
@@ -915,6 +919,12 @@ __device__ __forceinline__ void epilogue_tail(const CUtensorMap* tmOut, const Ge
                                               uint32_t release_bar, int lane) {
   // [column][row] within the part: for each column the warp's 32 rows are 128 contiguous
   // bytes, so every store and load below is one coalesced line per warp
+  if (row0 >= p.M) {  // none of this warp's rows is in C; the other half skips them too
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(release_bar);
+    return;
+  }
   const long long per_part = 32LL * BN;
   float* mine = p.tail_ws + ((static_cast<long long>(slot) * 2 + half) * 8 + part) * per_part +
                 lane;
