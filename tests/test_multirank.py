@@ -88,3 +88,18 @@ def test_traffic_rows_are_per_variant(tmp_path, monkeypatch):
     assert bench.traffic_from_profiles("square8192") == 100.0
     assert bench.traffic_from_profiles("square8192/w4") == 200.0
     assert bench.traffic_from_profiles("skinny") is None  # taken on another source
+
+
+def test_oracle_sample_sizing_is_bounded():
+    """The CPU-baseline leg and the reference arm size their oracle sample from a fixed plus
+    per-row calibration; the sample stays within 1..M rows and grows with the time budget."""
+    import bench
+    from fp16_gemm_relu_gb300 import workloads
+
+    wl = workloads.get("square256")
+    a, b = wl.make_a(), wl.make_b()
+    tiny = bench.sample_rows(wl, a, b, 1e-9)
+    big = bench.sample_rows(wl, a, b, 1e3)
+    assert tiny == 1
+    assert big == wl.M
+    assert 1 <= bench.sample_rows(wl, a, b, 0.05) <= wl.M
