@@ -119,6 +119,25 @@ def test_w4_decode_shape_sampled():
     check(got[np.ix_(rows, cols)], a, Wq[:, :], S, N, G, "relu", rows=rows, cols=cols)
 
 
+def test_w4_square_workload_sampled():
+    # the int4 bench workload at full size in its default launch (the CTA-pair kernel):
+    # square8192's A, weights and scales as the bench makes them, sampled rows and columns
+    # across tile and cluster boundaries
+    from fp16_gemm_relu_gb300 import workloads
+
+    wl = workloads.get("square8192")
+    M, N, K, G = wl.M, wl.N, wl.K, 128
+    a = wl.make_a()
+    Wq = inputs.int4_weights(K, N, wl.seed)
+    S = inputs.int4_scales(K // G, N, wl.seed, 1.0 / np.sqrt(K))
+    got = run_w4(a, Wq, S, N, G, act=1)
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], rng.integers(0, M, 40)]))
+    cols = np.unique(np.concatenate([[0, 7, 8, 127, 128, 255, 256, N - 1],
+                                     rng.integers(0, N, 40)]))
+    check(got[np.ix_(rows, cols)], a, Wq, S, N, G, "relu", rows=rows, cols=cols)
+
+
 @pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
 def test_w4_swapped_small_grid_ragged_fused_epilogue(act):
     # several tiles per CTA (2 and 3 CTAs for 6 column tiles), a ragged last tile (N = 700
