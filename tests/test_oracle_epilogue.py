@@ -5,6 +5,11 @@
 - GELU at points where the standard normal CDF is tabulated (Phi(1), Phi(2)).
 - Integer-valued inputs, bias and residual with relu: exact, so bitwise against int64 numpy.
 - The epilogue without bias/residual equals the plain relu / identity oracle bit for bit.
+- Both GELUs: act(x) - act(-x) = x (their non-linear part is odd), the tanh form within its
+  known 4.7e-4 error of x * Phi(x) computed with erf, and the limits act(0) = 0,
+  act(large x) = x, act(very negative x) = 0.  Planted in the oracle on the CPU, a wrong cubic
+  coefficient, sqrt(pi/2) for sqrt(2/pi), erf(x/2) for erf(x/sqrt 2) and a dropped tanh term
+  each fail at least one of these pins.
 """
 
 import math
@@ -91,3 +96,49 @@ def test_subgrid_and_argument_checks():
         oracle.gemm_epilogue(A, B, "relu", bias=bias[:-1])
     with pytest.raises(ValueError):
         oracle.gemm_epilogue(A, B, 7)
+
+
+def _ulp16(y):
+    return float(np.spacing(np.float16(abs(y)))) if y != 0 else 2.0 ** -24
+
+
+@pytest.mark.parametrize("act", ["gelu", "gelu_tanh"])
+def test_gelu_odd_part_identity(act):
+    # Both GELUs have the form x * (1 + h(x)) / 2 with h odd (erf or tanh of an odd
+    # polynomial), so act(x) - act(-x) = x exactly; each output is rounded once to fp16.
+    xs = np.array([0.125, 0.5, 0.75, 1.0, 1.5, 2.0, 3.0, 4.5, 7.0], np.float16)
+    bias = np.concatenate([xs, -xs])
+    A = np.zeros((1, 1), np.float16)
+    B = np.zeros((1, bias.size), np.float16)
+    out = oracle.gemm_epilogue(A, B, act, bias=bias)["out16_f64acc"].ravel().view(np.float16)
+    n = xs.size
+    for i, x in enumerate(xs.astype(np.float64)):
+        yp, ym = float(out[i]), float(out[n + i])
+        assert abs((yp - ym) - x) <= 0.5 * (_ulp16(yp) + _ulp16(ym)), (act, x, yp, ym)
+
+
+def test_gelu_tanh_approximates_exact_gelu():
+    # The tanh form approximates x * Phi(x) with a maximum absolute error of about 4.7e-4
+    # (near |x| = 2.2); Phi comes from math.erf, independent of tanh.  A wrong cubic
+    # coefficient (0.04 or 0.05 instead of 0.044715) or sqrt(pi/2) for sqrt(2/pi) exceeds the
+    # 6e-4 bound where the output's fp16 spacing is fine enough to show it.
+    xs = np.linspace(-6.0, 6.0, 97).astype(np.float16)
+    A = np.zeros((1, 1), np.float16)
+    B = np.zeros((1, xs.size), np.float16)
+    out = oracle.gemm_epilogue(A, B, "gelu_tanh", bias=xs)["out16_f64acc"].ravel().view(np.float16)
+    for x, y in zip(xs.astype(np.float64), out.astype(np.float64)):
+        exact = x * 0.5 * (1.0 + math.erf(x / math.sqrt(2.0)))
+        assert abs(y - exact) <= 6e-4 + 0.5 * _ulp16(y), (x, y, exact)
+
+
+def test_gelu_limits():
+    # gelu(0) = +0 or -0 (both compare equal to 0); for large x both forms return x; far left
+    # they vanish (|result| below the smallest fp16 subnormal rounds to a signed zero)
+    bias = np.array([0.0, 8.0, 12.0, 100.0, -30.0, -100.0], np.float16)
+    A = np.zeros((1, 1), np.float16)
+    B = np.zeros((1, bias.size), np.float16)
+    for act in ("gelu", "gelu_tanh"):
+        out = oracle.gemm_epilogue(A, B, act, bias=bias)["out16_f64acc"].ravel().view(np.float16)
+        assert float(out[0]) == 0.0
+        np.testing.assert_array_equal(out[1:4], bias[1:4])
+        assert float(out[4]) == 0.0 and float(out[5]) == 0.0
