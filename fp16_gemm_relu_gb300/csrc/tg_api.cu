@@ -667,6 +667,8 @@ cudaError_t bind_thread_context(int dev) {
   return e;
 }
 
+tg_status record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 tg_status device_info(int* sm_count, unsigned int** err) {
   DeviceState* ds = nullptr;
   tg_status st = current_device(&ds);

@@ -36,6 +36,10 @@ cudaError_t gemm_pair_max_clusters(int* out);
 // driver-API calls (tensor-map encoding) work from any host thread.
 cudaError_t bind_thread_context(int dev);
 
+// Records `e` as the calling thread's last CUDA error (what tg_last_cuda_error reports) and
+// returns TG_ERR_CUDA, for entry points defined outside tg_api.cu.
+tg_status record_cuda_error(cudaError_t e);
+
 // Current device's SM count and error word (checks the device; sets up library state).
 tg_status device_info(int* sm_count, unsigned int** err);
 

@@ -36,27 +36,29 @@ std::mutex g_setup_mutex;
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // One-time set-up for the current device: checks the device and looks up device addresses.
-// Allocates nothing.
+// Allocates nothing.  Every CUDA failure is recorded for tg_last_cuda_error.
 tg_status setup_current_device(StaticSetup** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TG_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return tg::record_cuda_error(e);
   if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED_DEVICE;
-  if (tg::bind_thread_context(dev) != cudaSuccess) return TG_ERR_CUDA;
+  if ((e = tg::bind_thread_context(dev)) != cudaSuccess) return tg::record_cuda_error(e);
   std::lock_guard<std::mutex> lock(g_setup_mutex);
   StaticSetup& s = g_setup[dev];
   if (!s.done) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return TG_ERR_CUDA;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return tg::record_cuda_error(e);
     if (major != 10 || minor != 3) {
       s.status = TG_ERR_UNSUPPORTED_DEVICE;
     } else {
       void* ws = nullptr;
-      if (cudaGetSymbolAddress(&ws, g_tg_static_workspace) != cudaSuccess) return TG_ERR_CUDA;
+      if ((e = cudaGetSymbolAddress(&ws, g_tg_static_workspace)) != cudaSuccess)
+        return tg::record_cuda_error(e);
       unsigned int* err = nullptr;
-      if (tg::error_word_address(&err) != cudaSuccess) return TG_ERR_CUDA;
+      if ((e = tg::error_word_address(&err)) != cudaSuccess) return tg::record_cuda_error(e);
       s.workspace = static_cast<float*>(ws);
       s.err = err;
       s.sm_count = sms;
@@ -66,6 +68,19 @@ tg_status setup_current_device(StaticSetup** out) {
   }
   *out = &s;
   return s.status;
+}
+
+// True when splits x M x ldw float32 values fit in the fixed workspace.  Each product is
+// checked by division first, so no intermediate can overflow (M and ldw may each approach
+// 2^31).
+bool fits_workspace(int64_t splits, int64_t M, int64_t ldw) {
+  const uint64_t limit = TG_STATIC_WORKSPACE_BYTES;
+  const uint64_t row = static_cast<uint64_t>(ldw) * 4u;  // ldw < 2^31: no overflow
+  if (row == 0 || row > limit) return false;
+  if (static_cast<uint64_t>(M) > limit / row) return false;
+  const uint64_t per_split = static_cast<uint64_t>(M) * row;  // <= limit
+  if (per_split == 0) return true;
+  return static_cast<uint64_t>(splits) <= limit / per_split;
 }
 
 CUresult encode(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, CUtensorMapDataType dt,
@@ -107,20 +122,18 @@ extern "C" tg_status tg_gemm_relu_f16_splitk_noalloc(const void* A, const void* 
   const int64_t kbps = kblocks > 0 ? cdiv(kblocks, std::min(want, kblocks)) : 1;
   const int64_t splits = kblocks > 0 ? cdiv(kblocks, kbps) : 1;  // every split is non-empty
   const int64_t ldw = cdiv(N, 4) * 4;
-  if (K > 0 && splits * M * ldw * 4 > static_cast<int64_t>(TG_STATIC_WORKSPACE_BYTES))
-    return TG_ERR_NO_WORKSPACE;
+  if (K > 0 && !fits_workspace(splits, M, ldw)) return TG_ERR_NO_WORKSPACE;
 
   StaticSetup* su = nullptr;
   tg_status st = setup_current_device(&su);
   if (st != TG_OK) return st;
   if (K == 0) {  // the empty sum: C = +0
-    return cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), stream) ==
-                   cudaSuccess
-               ? TG_OK
-               : TG_ERR_CUDA;
+    const cudaError_t e =
+        cudaMemset2DAsync(C, size_t(ldc) * 2, 0, size_t(N) * 2, size_t(M), stream);
+    return e == cudaSuccess ? TG_OK : tg::record_cuda_error(e);
   }
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-  if (!tg::tensor_map_encoder(&enc)) return TG_ERR_CUDA;
+  if (!tg::tensor_map_encoder(&enc)) return tg::record_cuda_error(cudaErrorNotSupported);
 
   tg::GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
@@ -139,7 +152,7 @@ extern "C" tg_status tg_gemm_relu_f16_splitk_noalloc(const void* A, const void* 
           CUDA_SUCCESS ||
       encode(enc, &L.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, su->workspace, 3, w_dims, w_str,
              w_box) != CUDA_SUCCESS)
-    return TG_ERR_CUDA;
+    return tg::record_cuda_error(cudaErrorInvalidValue);
 
   const int64_t tiles_m = cdiv(M, tg::kBM);
   const int64_t tiles_n = cdiv(N, kBlockN);
@@ -161,9 +174,10 @@ extern "C" tg_status tg_gemm_relu_f16_splitk_noalloc(const void* A, const void* 
   p.err = su->err;
   L.grid = static_cast<int>(std::min<int64_t>(units, su->sm_count));
   L.stream = stream;
-  if (tg::launch_gemm_bn256(L, /*out_f32=*/true) != cudaSuccess) return TG_ERR_CUDA;
-  if (tg::launch_splitk_reduce(su->workspace, ldw, M * ldw, static_cast<int>(splits), C, ldc, p,
-                               su->sm_count, stream) != cudaSuccess)
-    return TG_ERR_CUDA;
+  cudaError_t e = tg::launch_gemm_bn256(L, /*out_f32=*/true);
+  if (e != cudaSuccess) return tg::record_cuda_error(e);
+  e = tg::launch_splitk_reduce(su->workspace, ldw, M * ldw, static_cast<int>(splits), C, ldc, p,
+                               su->sm_count, stream);
+  if (e != cudaSuccess) return tg::record_cuda_error(e);
   return TG_OK;
 }

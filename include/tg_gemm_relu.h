@@ -239,14 +239,18 @@ tg_status tg_release_workspace(void);
  * re-entered, a runtime that has handed all device memory to its own arena, or
  * latency-critical work where an allocation could block or fail.
  *
- * It always takes the split-K path: `split_k` splits (clamped to 1..number of 64-wide K
- * blocks; 0 picks 2) each write a float32 partial tile into a fixed workspace, and a second
- * kernel adds the splits in order, applies the epilogue and writes fp16 C.  The workspace is
- * one array of TG_STATIC_WORKSPACE_BYTES bytes of device memory that is part of the library
- * itself: every GPU on which the library is used holds it until the process exits.
+ * It always takes the split-K path: the K range is cut into S_eff splits, each split writes a
+ * float32 partial tile into a fixed workspace, and a second kernel adds the splits in order,
+ * applies the epilogue and writes fp16 C.  The workspace is one array of
+ * TG_STATIC_WORKSPACE_BYTES bytes of device memory that is part of the library itself: every
+ * GPU on which the library is used holds it until the process exits.
  *
- *  - Needs split_k * M * (N rounded up to 4) * 4 bytes <= TG_STATIC_WORKSPACE_BYTES;
- *    larger problems return TG_ERR_NO_WORKSPACE before anything is launched.
+ *  - The effective split count: with kb = ceil(K / 64) K blocks and S = split_k (0 means 2)
+ *    clamped to 1..kb, each split takes ceil(kb / S) K blocks and S_eff = ceil(kb / ceil(kb /
+ *    S)) <= S splits are non-empty (for example kb = 10, S = 6 gives S_eff = 5).
+ *  - Needs S_eff * M * (N rounded up to 4) * 4 bytes <= TG_STATIC_WORKSPACE_BYTES (sizing
+ *    with split_k in place of S_eff is always enough); a larger need returns
+ *    TG_ERR_NO_WORKSPACE before anything is launched.  K == 0 needs no workspace (C = +0).
  *  - A and B must be 16-byte aligned with lda and ldb multiples of 8 (TG_ERR_MISALIGNED
  *    otherwise); C only needs 2-byte alignment.  Other arguments as for tg_gemm_relu_f16.
  *  - The first call on each device does a one-time set-up with that device current (it

@@ -181,3 +181,26 @@ def test_plan_tail_split(lib):
     assert _plan(300, 600, 1500, options={"pair": 1, "tail": 1, "max_ctas": 6})["tail_tiles"] == 0
     assert _plan(300, 600, 1500, options={"pair": 1, "tail": 1, "max_ctas": 8})["tail_tiles"] == 2
     assert _plan(8192, 8192, 8192, options={"split_k": 2, "tail": 1})["tail_tiles"] == 0
+
+
+def test_noalloc_workspace_bound_cannot_overflow(lib):
+    # The fixed-workspace entry point refuses, on the host and before any device work, every
+    # problem whose split partials exceed its array.  Shapes near the 2^31 dimension limit make
+    # splits * M * ldw * 4 exceed 2^64, which a plain product would wrap past the bound.
+    big = (1 << 31) - 1024
+    p = 4096
+    cases = [
+        (big, big, 64, 1),          # M * ldw * 4 ~ 2^64
+        (big, 8, 64 * 8, 8),        # splits x a per-split slice just over 2^34
+        (1, big, 64, 1),            # one row wider than the array
+        (4096, 4096, 1024, 2),      # 128 MiB of partials against 64 MiB
+    ]
+    for M, N, K, split in cases:
+        st = binding.tg_gemm_relu_f16_splitk_noalloc(p, p, p, M, N, K, -(-K // 8) * 8,
+                                                     -(-N // 8) * 8, N, 1, split, 0)
+        assert st == binding.TG_ERR_NO_WORKSPACE, (M, N, K, split, st)
+    # argument errors come first, also without a device
+    assert binding.tg_gemm_relu_f16_splitk_noalloc(p, p, p, 4, 4, 4, 8, 8, 4, 1, -1, 0) == \
+        binding.TG_ERR_INVALID_ARG
+    assert binding.tg_gemm_relu_f16_splitk_noalloc(p, p, p, 4, 4, 4, 8, 8, 3, 1, 1, 0) == \
+        binding.TG_ERR_INVALID_ARG
