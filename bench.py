@@ -52,6 +52,10 @@ def parse_args():
                     help="relu: the metric's path; the others time the fused bias/GELU/residual "
                          "epilogue on the same GEMM")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip timing the other named workloads (the 'workloads' block)")
+    ap.add_argument("--workload-seconds", type=float, default=0.5,
+                    help="minimum wall time of each other workload's timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target seconds of oracle work for the cpu_baseline sample")
@@ -284,6 +288,132 @@ def run_reference(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def timed_steps(torch, step, stream, steps, scrub=None, sampler=None):
+    """Runs `steps` calls of step() on `stream`, each bracketed by CUDA events; with `scrub`
+    (a buffer larger than L2) it is rewritten between steps, outside the step's events.
+    Returns (per-step ms, ms of the whole region)."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if sampler is not None:
+        sampler.start()
+    t0.record(stream)
+    for i in range(steps):
+        if scrub is not None:
+            scrub.fill_(1.0)  # L2 flush between timed steps, outside the step's events
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    stream.synchronize()
+    if sampler is not None:
+        sampler.stop()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], t0.elapsed_time(t1)
+
+
+def clock_soak(torch, step, stream, scrub, bus, seconds):
+    """Clock record of the step run back to back for about `seconds` (outside any timed
+    region): what the sampler sees of the GPU under this load."""
+    _, probe_ms = timed_steps(torch, step, stream, 3, scrub)
+    n = int(min(max(3, seconds * 1e3 / max(probe_ms / 3, 1e-3)), 100000))
+    sampler = ClockSampler(bus)
+    _, region_ms = timed_steps(torch, step, stream, n, scrub, sampler)
+    out = sampler.summary()
+    out.update(steps=n, region_ms=region_ms)
+    return out
+
+
+def roofline(flops, alg_bytes, flops_per_step, kernel_ms, peaks, peak_src):
+    """Bound (the slower of dense fp16 tensor time and algorithmic bytes over HBM), achieved
+    rate per step and its fraction of the measured peak."""
+    t_tensor = flops / (peaks["bf16_tflops"] * FP16_OVER_BF16 * 1e12)
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flops_per_step / (kernel_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops"] * FP16_OVER_BF16, "unit": "TFLOP/s"}
+    else:
+        achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json bf16 burst x {FP16_OVER_BF16} "
+                           "fp16/bf16 nominal ratio)" if roof["bound"] == "tensor"
+                           else f"{peak_src} (MEASURED_PEAKS.json copy bandwidth)")
+    roof["kernel_ms"] = kernel_ms
+    roof["t_roof_ms"] = 1e3 * max(t_tensor, t_hbm)
+    return roof
+
+
+def other_workloads(args, headline, lib, binding, dev, stream, bus, peaks, peak_src):
+    """The other named workloads, each timed like the headline (W warm-up steps, CUDA events
+    per step on the launching stream, L2 flushed between steps when the operands fit in it)
+    for at least `args.workload_seconds` of wall time, with its own clock record."""
+    import torch
+
+    import fp16_gemm_relu_gb300 as tg
+
+    props = torch.cuda.get_device_properties(dev)
+    out = {}
+    for name in workloads.ORDER:
+        if name == headline:
+            continue
+        wl = workloads.get(name)
+        A = torch.from_numpy(wl.make_a()).to(dev)
+        B = torch.from_numpy(wl.make_b()).to(dev)
+        C = torch.empty((wl.M, wl.N), dtype=torch.float16, device=dev)
+        plan = tg.plan(wl.M, wl.N, wl.K, num_sms=props.multi_processor_count,
+                       a_ptr=A.data_ptr(), b_ptr=B.data_ptr(), c_ptr=C.data_ptr())
+        in_bytes = wl.algorithmic_bytes - 2 * wl.M * wl.N
+        scrub = (torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+                 if in_bytes <= L2_BYTES else None)
+
+        def step():
+            st = lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
+                                      wl.K, wl.N, wl.N, binding.TG_EPILOGUE_RELU, stream.cuda_stream)
+            if st != 0:
+                raise binding.TgError(st, "tg_gemm_relu_f16")
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                if scrub is not None:
+                    scrub.fill_(1.0)
+                step()
+            _, probe_ms = timed_steps(torch, step, stream, 3, scrub)
+            steps = int(min(max(args.steps, args.workload_seconds * 1e3 / max(probe_ms / 3, 1e-3)),
+                            100000))
+            sampler = ClockSampler(bus)
+            step_ms, region_ms = timed_steps(torch, step, stream, steps, scrub, sampler)
+        st, word = binding.tg_device_error_check(clear=True)
+        if st != 0:
+            raise RuntimeError(f"device error word {word:#x} after workload {name}")
+        ms = statistics.mean(step_ms)
+        roof = roofline(wl.flops, wl.algorithmic_bytes, wl.flops, ms, peaks, peak_src)
+        clocks = sampler.summary()
+        entry = {
+            "M": wl.M, "N": wl.N, "K": wl.K, "steps": steps, "ms_per_step": ms,
+            "value": wl.flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "roofline": {k: roof[k] for k in ("bound", "achieved", "unit", "peak", "frac",
+                                               "t_roof_ms")},
+            "kernel_ms": ms if plan["kernels"] == 1 else None,
+            "step_kernels": plan["kernels"],
+            "plan": {k: plan[k] for k in ("block_m", "block_n", "split_k", "tail_tiles",
+                                          "repack_a", "repack_b", "workspace_epilogue", "grid",
+                                          "cta_pair") if k in plan},
+            "l2": "flushed between steps" if scrub is not None else "operands larger than L2",
+            "clocks": clocks, "region_ms": region_ms,
+        }
+        if clocks.get("sm_mhz"):
+            entry["sm_cycles_per_step"] = ms * 1e-3 * clocks["sm_mhz"] * 1e6
+        if plan["kernels"] > 1:
+            entry["note"] = ("frac is the whole step (operand repack, GEMM and split-K "
+                             "reduction) against the GEMM's roofline")
+        out[name] = entry
+        del A, B, C, scrub
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl):
     import torch
 
@@ -415,26 +545,10 @@ def run_ours(args, wl):
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        sampler.start()
-        t_all0 = torch.cuda.Event(enable_timing=True)
-        t_all1 = torch.cuda.Event(enable_timing=True)
-        t_all0.record(stream)
-        for i in range(args.steps):
-            if flush:
-                scrub.fill_(1.0)  # L2 flush between timed steps, outside the step's events
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        t_all1.record(stream)
-        stream.synchronize()
-        sampler.stop()
+        step_ms, region_ms = timed_steps(torch, step, stream, args.steps, scrub, sampler)
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    region_ms = t_all0.elapsed_time(t_all1)
     total_ms = sum(step_ms) if flush else region_ms
     total_ms = slowest_rank_ms(total_ms, device=dev)
     ms_per_step = total_ms / args.steps
@@ -442,35 +556,30 @@ def run_ours(args, wl):
     st, word = binding.tg_device_error_check(clear=True)
     if st != 0:
         raise RuntimeError(f"device error word {word:#x} after the timed region")
+    clocks = sampler.summary()
+    clocks["region_ms"] = region_ms
+    if region_ms < 500.0:
+        # the timed region is too short for the clock sampler to see the GPU under load: run the
+        # same step back to back for ~0.5 s more (after the timed region, outside it) and report
+        # what the sampler saw there too
+        clocks["soak"] = clock_soak(torch, step, stream, scrub, bus, 0.5)
+    if clocks.get("sm_mhz"):
+        clocks["sm_cycles_per_step"] = ms_per_step * 1e-3 * clocks["sm_mhz"] * 1e6
 
     # roofline of the dominant kernel (the tcgen05 GEMM); one launch per step when the plan has
     # a single kernel, so the per-step events bracket exactly that kernel
     peaks, peak_src = load_peaks()
     kernel_ms = statistics.mean(step_ms)
-    t_tensor = wl.flops / (peaks["bf16_tflops"] * FP16_OVER_BF16 * 1e12)
-    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
-    if t_tensor >= t_hbm:
-        achieved = flops_per_step / (kernel_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops"] * FP16_OVER_BF16, "unit": "TFLOP/s"}
-    else:
-        achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = roofline(wl.flops, alg_bytes, flops_per_step, kernel_ms, peaks, peak_src)
     roof["traffic"] = (traffic_from_profiles(traffic_key(wl.name, args.pass_, args.epilogue,
                                                          args.dequant))
                        if plan["kernels"] == 1 else None)
-    roof["peak_source"] = (f"{peak_src} (MEASURED_PEAKS.json bf16 burst x {FP16_OVER_BF16} "
-                           "fp16/bf16 nominal ratio)" if roof["bound"] == "tensor"
-                           else f"{peak_src} (MEASURED_PEAKS.json copy bandwidth)")
     if roof["bound"] == "tensor" and "bf16_tflops_sustained" in peaks:
         # context only: the cuBLAS rate measured in a seconds-long loop under the power cap
         # (MEASURED_PEAKS.json's sustained figure; the bench's back-to-back steps run in the
         # same regime)
         roof["peak_sustained"] = peaks["bf16_tflops_sustained"] * FP16_OVER_BF16
         roof["frac_of_sustained"] = roof["achieved"] / roof["peak_sustained"]
-    roof["kernel_ms"] = kernel_ms
-    roof["t_roof_ms"] = 1e3 * max(t_tensor, t_hbm)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -488,8 +597,12 @@ def run_ours(args, wl):
                                                  "kernels", "kernel") if k in plan}},
         "gpu_launches": args.steps * plan["kernels"],
         "roofline": roof,
-        "clocks": sampler.summary(),
+        "clocks": clocks,
     }
+    if (rank == 0 and not args.no_workloads and args.pass_ == "forward"
+            and args.epilogue == "relu" and args.dequant == "none"):
+        line["workloads"] = other_workloads(args, wl.name, lib, binding, dev, stream, bus, peaks,
+                                            peak_src)
 
     if rank == 0 and not args.no_e2e and args.pass_ == "forward" and args.dequant == "none":
         line["e2e"] = e2e(wl, A_h, B_h, dev, max(3, min(args.steps, 10)))

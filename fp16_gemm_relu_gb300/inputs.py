@@ -27,7 +27,7 @@ import numpy as np
 GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 23
+_CHUNK = 1 << 22
 
 TENSOR_A = 0
 TENSOR_B = 1
@@ -56,30 +56,48 @@ def raw_u64(key: np.uint64, start: int, count: int) -> np.ndarray:
         return mix64(key + e * GAMMA)
 
 
+def _fill_chunk(out: np.ndarray, start: int, n: int, k0: np.uint64, k1: np.uint64, dist: str,
+                scale: float) -> None:
+    x = raw_u64(k0, start, n)
+    if dist == "uniform":
+        v = (x >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
+        v = 2.0 * v - 1.0
+    elif dist == "normal":
+        x2 = raw_u64(k1, start, n)
+        u1 = 1.0 - (x >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        u2 = (x2 >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+        v = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+    elif dist == "int":
+        # integers in [-2, 2]: every partial sum of a dot product stays exact in fp32
+        v = ((x >> np.uint64(32)) % np.uint64(5)).astype(np.float64) - 2.0
+    else:
+        raise ValueError(f"unknown distribution {dist!r}")
+    if scale != 1.0:
+        v = v * scale
+    out[start:start + n] = v.astype(np.float16)
+
+
 def _fill(rows: int, cols: int, seed: int, tensor: int, dist: str, scale: float) -> np.ndarray:
+    if dist not in ("uniform", "normal", "int"):
+        raise ValueError(f"unknown distribution {dist!r}")
     total = rows * cols
     out = np.empty(total, dtype=np.float16)
     k0 = stream_key(seed, tensor, 0)
     k1 = stream_key(seed, tensor, 1)
-    for start in range(0, total, _CHUNK):
-        n = min(_CHUNK, total - start)
-        x = raw_u64(k0, start, n)
-        if dist == "uniform":
-            v = (x >> np.uint64(40)).astype(np.float64) * (2.0 ** -24)
-            v = 2.0 * v - 1.0
-        elif dist == "normal":
-            x2 = raw_u64(k1, start, n)
-            u1 = 1.0 - (x >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-            u2 = (x2 >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
-            v = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
-        elif dist == "int":
-            # integers in [-2, 2]: every partial sum of a dot product stays exact in fp32
-            v = ((x >> np.uint64(32)) % np.uint64(5)).astype(np.float64) - 2.0
-        else:
-            raise ValueError(f"unknown distribution {dist!r}")
-        if scale != 1.0:
-            v = v * scale
-        out[start:start + n] = v.astype(np.float16)
+    starts = list(range(0, total, _CHUNK))
+    if len(starts) <= 1:
+        for start in starts:
+            _fill_chunk(out, start, min(_CHUNK, total - start), k0, k1, dist, scale)
+    else:
+        # chunks are independent slices of the counter-based stream: drawing them on several
+        # threads (numpy releases the GIL in these loops) gives the same values as in order
+        import concurrent.futures as cf
+        import os
+
+        workers = min(len(starts), os.cpu_count() or 1, 16)
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            list(ex.map(lambda st: _fill_chunk(out, st, min(_CHUNK, total - st), k0, k1, dist,
+                                               scale), starts))
     return out.reshape(rows, cols)
 
 
