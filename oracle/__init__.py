@@ -45,6 +45,10 @@ def lib() -> ctypes.CDLL:
                                               ctypes.c_int, p, p, i64, p, p, p, ctypes.c_int]
         L.tg_oracle_dequant_w4.restype = ctypes.c_int
         L.tg_oracle_dequant_w4.argtypes = [p, p, i64, i64, i64, i64, i64, p]
+        L.tg_oracle_dequant_nf4.restype = ctypes.c_int
+        L.tg_oracle_dequant_nf4.argtypes = [p, p, i64, i64, i64, i64, i64, p]
+        L.tg_oracle_nf4_code.restype = ctypes.c_double
+        L.tg_oracle_nf4_code.argtypes = [ctypes.c_int]
         L.tg_oracle_max_threads.restype = ctypes.c_int
         L.tg_oracle_max_threads.argtypes = []
         _lib = L
@@ -174,6 +178,25 @@ def dequant_w4(Wq, scales, K: int, N: int, group: int) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     return out.view(np.float16)
+
+
+def dequant_nf4(Wq, scales, K: int, N: int, group: int) -> np.ndarray:
+    """fp16 K x N weights from packed NF4 codes Wq (K x ceil(N/8) uint32, same packing as
+    dequant_w4) and fp16 scales (ceil(K/group) x N):
+    w = fp16_rne(fp16_rne(nf4[q]) * s), nf4 the QLoRA code table.  See tg_oracle.c."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
+    sc = np.ascontiguousarray(scales, dtype=np.float16).view(np.uint16)
+    out = np.empty((K, N), np.uint16)
+    rc = lib().tg_oracle_dequant_nf4(_ptr(Wq), _ptr(sc), K, N, Wq.shape[1], sc.shape[1], group,
+                                     _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return out.view(np.float16)
+
+
+def nf4_codes() -> np.ndarray:
+    """The 16 NF4 code values the oracle uses (float64, as printed in QLoRA's Appendix E)."""
+    return np.array([lib().tg_oracle_nf4_code(q) for q in range(16)], dtype=np.float64)
 
 
 def relu_backward(dC, C) -> np.ndarray:

@@ -259,3 +259,57 @@ int tg_oracle_dequant_w4(const uint32_t* Wq, const uint16_t* scales, int64_t K, 
   }
   return 0;
 }
+
+/* ---- NF4 weight dequantisation (W_NF4 / A_FP16 GEMM) ----
+ *
+ * The paper-reading page (section 5) names a second dequantising GEMM beside W_INT4 / A_FP16:
+ * 4-bit NormalFloat weights with fp16 activations.  NF4 (Dettmers, Pagnoni, Holtzman and
+ * Zettlemoyer, "QLoRA: Efficient Finetuning of Quantized LLMs", NeurIPS 2023, section 3 and
+ * Appendix E) maps a 4-bit code q to one of 16 values spread like the quantiles of a standard
+ * normal distribution, normalised to [-1, 1], with an exact zero.  The table below is the one
+ * printed in that appendix.
+ *
+ * Storage, the same as the int4 format above: Wq holds K rows of ceil(N/8) uint32 words;
+ * column 8c+e of row k is the nibble in bits [4e, 4e+4) of word (k, c).  scales holds
+ * ceil(K/group) rows of N fp16 values (leading dimension lds).  The weight is
+ *     w[k][n] = fp16_rne( fp16_rne(nf4[q[k][n]]) * scales[k / group][n] )
+ * the code value rounded to fp16 once (it is held in the activations' precision), then the
+ * product (exact in double) rounded once.  out16 is K x N fp16 bits, row-major.
+ */
+static const double kNf4Codes[16] = {
+    -1.0,
+    -0.6961928009986877,
+    -0.5250730514526367,
+    -0.39491748809814453,
+    -0.28444138169288635,
+    -0.18477343022823334,
+    -0.09105003625154495,
+    0.0,
+    0.07958029955625534,
+    0.16093020141124725,
+    0.24611230194568634,
+    0.33791524171447754,
+    0.44070982933044434,
+    0.5626170039176941,
+    0.7229568362236023,
+    1.0,
+};
+
+/* The NF4 code value of q (0..15) as printed; NaN for any other q. */
+double tg_oracle_nf4_code(int q) { return (q >= 0 && q < 16) ? kNf4Codes[q] : NAN; }
+
+int tg_oracle_dequant_nf4(const uint32_t* Wq, const uint16_t* scales, int64_t K, int64_t N,
+                          int64_t ldq, int64_t lds, int64_t group, uint16_t* out16) {
+  if (K < 0 || N < 0 || group <= 0 || ldq < (N + 7) / 8 || lds < N) return -1;
+  for (int64_t k = 0; k < K; ++k) {
+    const int64_t g = k / group; /* scale row */
+    for (int64_t n = 0; n < N; ++n) {
+      const uint32_t word = Wq[k * ldq + n / 8];
+      const unsigned nib = (word >> (4u * (uint32_t)(n % 8))) & 15u;
+      const double code = tg_oracle_f16_to_f64(tg_oracle_f64_to_f16(kNf4Codes[nib]));
+      const double s = tg_oracle_f16_to_f64(scales[g * lds + n]);
+      out16[k * N + n] = tg_oracle_f64_to_f16(code * s);
+    }
+  }
+  return 0;
+}

@@ -51,6 +51,26 @@ MUTANTS = {
         "tg_oracle.c",
         "scales[(k / group) * lds + n]",
         "scales[(k / group) * lds + (n + 1 < N ? n + 1 : n)]"),
+    "nf4 codes 12 and 13 swapped": (
+        "tg_oracle.c",
+        "    0.44070982933044434,\n    0.5626170039176941,",
+        "    0.5626170039176941,\n    0.44070982933044434,"),
+    "nf4 code 3 mistyped": (
+        "tg_oracle.c",
+        "-0.39491748809814453,",
+        "-0.39591748809814453,"),
+    "nf4 code used at full precision in the product": (
+        "tg_oracle.c",
+        "tg_oracle_f16_to_f64(tg_oracle_f64_to_f16(kNf4Codes[nib]))",
+        "kNf4Codes[nib]"),
+    "nf4 nibble order reversed": (
+        "tg_oracle.c",
+        "(word >> (4u * (uint32_t)(n % 8))) & 15u",
+        "(word >> (4u * (uint32_t)(7 - n % 8))) & 15u"),
+    "nf4 scale group of half the rows": (
+        "tg_oracle.c",
+        "const int64_t g = k / group; /* scale row */",
+        "const int64_t g = k / (group > 1 ? group / 2 : 1);"),
     "GELU-tanh cubic coefficient 0.05": (
         "tg_oracle.c",
         "0.044715 * x * x * x",
