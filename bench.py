@@ -46,8 +46,9 @@ def parse_args():
     ap.add_argument("--pass", dest="pass_", default="forward", choices=["forward", "backward"],
                     help="backward: one step = dZ = relu'(C) * dC, dA = dZ B^T, dB = A^T dZ "
                          "(4MNK flops), all in the library's kernels")
-    ap.add_argument("--dequant", default="none", choices=["none", "w4"],
-                    help="w4: B is int4 weights (group 128 scales) decoded inside the GEMM")
+    ap.add_argument("--dequant", default="none", choices=["none", "w4", "nf4"],
+                    help="w4 / nf4: B is int4 / NF4 weights (group 128 scales) decoded inside "
+                         "the GEMM")
     ap.add_argument("--epilogue", default="relu", choices=["relu", "bias_gelu", "bias_relu_residual"],
                     help="relu: the metric's path; the others time the fused bias/GELU/residual "
                          "epilogue on the same GEMM")
@@ -447,7 +448,7 @@ def run_ours(args, wl):
 
     flops_per_step = wl.flops
     alg_bytes = wl.algorithmic_bytes
-    if args.dequant == "w4":
+    if args.dequant in ("w4", "nf4"):
         from fp16_gemm_relu_gb300 import inputs as _inputs
 
         G = 128
@@ -471,14 +472,14 @@ def run_ours(args, wl):
         else:
             plan = {"block_m": 256, "block_n": 256, "block_k": 64,
                     "kernel": "tg_gemm_w4_pair_kernel"}
-        plan.update({"split_k": 1, "kernels": 1, "dequant": "w4 g128"})
+        plan.update({"split_k": 1, "kernels": 1, "dequant": f"{args.dequant} g128"})
+        dq_fn = lib.tg_gemm_w4a16_f16 if args.dequant == "w4" else lib.tg_gemm_nf4a16_f16
 
         def step():
-            st = lib.tg_gemm_w4a16_f16(A.data_ptr(), Wq.data_ptr(), Sc.data_ptr(), C.data_ptr(),
-                                       wl.M, wl.N, wl.K, wl.K, ldq, wl.N, wl.N, G, None, None,
-                                       handle)
+            st = dq_fn(A.data_ptr(), Wq.data_ptr(), Sc.data_ptr(), C.data_ptr(), wl.M, wl.N, wl.K,
+                       wl.K, ldq, wl.N, wl.N, G, None, None, handle)
             if st != 0:
-                raise binding.TgError(st, "tg_gemm_w4a16_f16")
+                raise binding.TgError(st, f"dequantising GEMM ({args.dequant})")
     elif args.pass_ == "backward":
         # gradients of C = relu(A·B) for a seeded dC; the step is mask + two GEMMs
         from fp16_gemm_relu_gb300 import inputs as _inputs

@@ -99,6 +99,7 @@ def load_library() -> ctypes.CDLL:
         L.tg_relu_backward_f16.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, vp]
         L.tg_gemm_w4a16_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, ci,
                                         ctypes.POINTER(tg_epilogue), ctypes.POINTER(tg_options), vp]
+        L.tg_gemm_nf4a16_f16.argtypes = L.tg_gemm_w4a16_f16.argtypes
         L.tg_plan_query.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, ci,
                                     ctypes.POINTER(tg_options), ctypes.POINTER(tg_plan)]
         L.tg_device_error_check.argtypes = [ctypes.POINTER(ctypes.c_uint), ci]
@@ -110,6 +111,7 @@ def load_library() -> ctypes.CDLL:
         for name in ("tg_gemm_relu_f16", "tg_gemm_relu_f16_ex", "tg_gemm_relu_f16_host",
                      "tg_gemm_relu_f16_splitk_noalloc", "tg_gemm_f16_epilogue",
                      "tg_gemm_f16_t", "tg_relu_backward_f16", "tg_gemm_w4a16_f16",
+                     "tg_gemm_nf4a16_f16",
                      "tg_plan_query", "tg_device_error_check", "tg_last_cuda_error",
                      "tg_release_workspace", "tg_version"):
             getattr(L, name).restype = ci
@@ -171,6 +173,17 @@ def tg_gemm_w4a16_f16(A: int, Wq: int, scales: int, C: int, M: int, N: int, K: i
     return load_library().tg_gemm_w4a16_f16(A, Wq, scales, C, M, N, K, lda, ldq, lds, ldc,
                                             group_size, ctypes.byref(e), _opts(options),
                                             stream or None)
+
+
+def tg_gemm_nf4a16_f16(A: int, Wq: int, scales: int, C: int, M: int, N: int, K: int, lda: int,
+                       ldq: int, lds: int, ldc: int, group_size: int,
+                       activation: int = TG_ACT_NONE, bias: int = 0, residual: int = 0,
+                       ldr: int = 0, options=None, stream: int = 0) -> int:
+    """C = fp16(epilogue(A · W)) with NF4 weights decoded in the kernel (format in the header)."""
+    e = tg_epilogue(activation, bias or None, residual or None, ldr)
+    return load_library().tg_gemm_nf4a16_f16(A, Wq, scales, C, M, N, K, lda, ldq, lds, ldc,
+                                             group_size, ctypes.byref(e), _opts(options),
+                                             stream or None)
 
 
 def tg_relu_backward_f16(dC: int, C: int, dZ: int, M: int, N: int, lddc: int, ldc: int,

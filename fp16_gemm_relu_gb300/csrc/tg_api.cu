@@ -219,7 +219,11 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
       const int64_t waves = cdiv(units, grid);
       const bool ws = s_eff > 1 || !c_direct;
       const double kb_cycles = pair ? 512.0 : kblock_cycles(bn);
-      const double t_mma = double(waves) * double(kbps) * kb_cycles / clk;
+      // the pair kernel's cluster launch and its first 64 KB stage per CTA cost ~2 us more
+      // before the first MMA than the single-CTA kernel's start (measured on 2048^3, one wave
+      // either way: 22.6 us against 20.5 us)
+      const double t_start = pair ? 2.1e-6 : 0.0;
+      const double t_mma = double(waves) * double(kbps) * kb_cycles / clk + t_start;
       double slots = 0.0;  // wave-by-wave occupancy penalty on the memory time
       for (int64_t wv = 0; wv < waves; ++wv) {
         const int64_t active = (pair ? 2 : 1) * std::min<int64_t>(grid, units - wv * grid);
@@ -275,17 +279,19 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
 
   int64_t off = 0;
   if (P.repack_a) {  // A is stored (ta ? K x M : M x K)
-    pl.lda_p = round_up(ta ? M : K, 8);
+    // rows of the copies start on 128-byte lines: a 128-byte TMA box row then reads four
+    // 32-byte sectors of L2, where a row only 16-byte aligned spans five
+    pl.lda_p = round_up(ta ? M : K, 64);
     pl.off_a = off;
     off += round_up((ta ? K : M) * pl.lda_p * 2, 256);
   }
   if (P.repack_b) {  // B is stored (tb ? N x K : K x N)
-    pl.ldb_p = round_up(tb ? K : N, 8);
+    pl.ldb_p = round_up(tb ? K : N, 64);
     pl.off_b = off;
     off += round_up((tb ? N : K) * pl.ldb_p * 2, 256);
   }
   if (P.workspace_epilogue) {
-    pl.ldw = round_up(N, 4);
+    pl.ldw = round_up(N, 32);  // 128-byte rows for the same reason
     pl.off_w = off;
     off += round_up(int64_t(P.split_k) * M * pl.ldw * 4, 256);
   }

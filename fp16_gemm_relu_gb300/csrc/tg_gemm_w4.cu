@@ -10,10 +10,10 @@ namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int BMT>
+template <int BMT, int FMT>
 cudaError_t launch_w4t(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
                        const tg::GemmParams& p, int grid, cudaStream_t stream) {
-  auto kern = tg::tg_gemm_w4t_kernel<BMT>;
+  auto kern = tg::tg_gemm_w4t_kernel<BMT, FMT>;
   constexpr int smem = tg::W4TCfg<BMT>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -21,11 +21,11 @@ cudaError_t launch_w4t(const CUtensorMap& a, const CUtensorMap& q, const CUtenso
   return cudaGetLastError();
 }
 
-template <int BN>
+template <int BN, int FMT>
 cudaError_t launch_w4(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
                       const CUtensorMap& out, const tg::GemmParams& p, int grid,
                       cudaStream_t stream) {
-  auto kern = tg::tg_gemm_w4_kernel<BN>;
+  auto kern = tg::tg_gemm_w4_kernel<BN, FMT>;
   constexpr int smem = tg::W4Cfg<BN>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -35,14 +35,15 @@ cudaError_t launch_w4(const CUtensorMap& a, const CUtensorMap& q, const CUtensor
 
 int w4_pair_query_clusters();
 
+template <int FMT>
 cudaError_t launch_w4_pair(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
                            const CUtensorMap& out, const tg::GemmParams& p, int grid,
                            cudaStream_t stream) {
   constexpr int smem = tg::W4PairCfg::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(tg::tg_gemm_w4_pair_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = tg::tg_gemm_w4_pair_kernel<FMT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  tg::tg_gemm_w4_pair_kernel<<<grid, tg::W4PairCfg::kThreads, smem, stream>>>(a, q, s, out, p);
+  kern<<<grid, tg::W4PairCfg::kThreads, smem, stream>>>(a, q, s, out, p);
   return cudaGetLastError();
 }
 
@@ -65,8 +66,10 @@ int w4_pair_max_clusters() {
 
 int w4_pair_query_clusters() {
   constexpr int smem = tg::W4PairCfg::kSmemBytes;
-  if (cudaFuncSetAttribute(tg::tg_gemm_w4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess) {
+  // both formats' instances use the same threads and shared memory
+  auto kern = tg::tg_gemm_w4_pair_kernel<tg::kFmtInt4>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -82,8 +85,8 @@ int w4_pair_query_clusters() {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(tg::tg_gemm_w4_pair_kernel),
-                                     &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(kern), &cfg) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -102,13 +105,13 @@ CUresult encode(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m, CUtensorM
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-}  // namespace
-
-extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales,
-                                       void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                                       int64_t ldq, int64_t lds, int64_t ldc, int group_size,
-                                       const tg_epilogue* epi, const tg_options* opt,
-                                       tg_stream_t stream_) {
+// Both dequantising GEMMs (int4 and NF4 weights): same packing, arguments and plans; only
+// the per-nibble decode in the kernels differs.
+template <int FMT>
+tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C, int64_t M,
+                      int64_t N, int64_t K, int64_t lda, int64_t ldq, int64_t lds, int64_t ldc,
+                      int group_size, const tg_epilogue* epi, const tg_options* opt,
+                      tg_stream_t stream_) {
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const int64_t max_dim = (int64_t{1} << 31) - 1024;
   if (M < 0 || N < 0 || K < 0 || M > max_dim || N > max_dim || K > max_dim)
@@ -146,7 +149,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
   tg_status st = tg::device_info(&sms, &err);
   if (st != TG_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-  if (!tg::tensor_map_encoder(&enc)) return TG_ERR_CUDA;
+  if (!tg::tensor_map_encoder(&enc)) return tg::record_cuda_error(cudaErrorNotSupported);
 
   const int grid_cap0 = o.max_ctas > 0 ? std::min(o.max_ctas, sms) : sms;
   const bool swap = o.swap_ab > 0 || (o.swap_ab == 0 && M <= 128);
@@ -163,7 +166,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
         encode(enc, &ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, scales, uint64_t(N),
                uint64_t(cdiv(K, group_size)), uint64_t(lds) * 2, 128, 1,
                CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
-      return TG_ERR_CUDA;
+      return tg::record_cuda_error(cudaErrorInvalidValue);
     tg::GemmParams p;
     std::memset(&p, 0, sizeof(p));
     p.tiles_m = static_cast<int>(tm);
@@ -176,6 +179,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
     p.act = e.activation;
     p.group_kb = group_size / tg::kBK;
     p.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : 2000);
+    p.debug_flags = o.debug_flags;
     p.err = err;
     p.c = static_cast<__half*>(C);
     p.ldc = ldc;
@@ -203,16 +207,18 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
       p.units = static_cast<int>(tiles + r);
       p.tail_ws = reinterpret_cast<float*>(scratch);
       p.tail_cnt = reinterpret_cast<int*>(scratch + cnt_off);
-      if (cudaMemsetAsync(p.tail_cnt, 0, size_t(r) * 4 * sizeof(int), stream) != cudaSuccess) {
+      const cudaError_t me = cudaMemsetAsync(p.tail_cnt, 0, size_t(r) * 4 * sizeof(int), stream);
+      if (me != cudaSuccess) {
         cudaFreeAsync(scratch, stream);
-        return TG_ERR_CUDA;
+        return tg::record_cuda_error(me);
       }
     }
     const int grid = static_cast<int>(std::min<int64_t>(p.units, grid_cap0));
-    const cudaError_t ce = bmt == 64 ? launch_w4t<64>(ta, tq, ts, p, grid, stream)
-                                     : launch_w4t<128>(ta, tq, ts, p, grid, stream);
-    if (scratch && cudaFreeAsync(scratch, stream) != cudaSuccess) return TG_ERR_CUDA;
-    return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    const cudaError_t ce = bmt == 64 ? launch_w4t<64, FMT>(ta, tq, ts, p, grid, stream)
+                                     : launch_w4t<128, FMT>(ta, tq, ts, p, grid, stream);
+    const cudaError_t fe = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
+    if (ce != cudaSuccess) return tg::record_cuda_error(ce);
+    return fe == cudaSuccess ? TG_OK : tg::record_cuda_error(fe);
   }
 
   // many rows: 256 x 256 tiles on CTA pairs, each CTA decoding half of the weight tile
@@ -237,7 +243,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
         encode(enc, &tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C,
                uint64_t(std::max<int64_t>(N & ~int64_t{7}, 8)), uint64_t(M), uint64_t(ldc) * 2, 64,
                32, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return TG_ERR_CUDA;
+      return tg::record_cuda_error(cudaErrorInvalidValue);
     tg::GemmParams p;
     std::memset(&p, 0, sizeof(p));
     p.tiles_m = static_cast<int>(tm);
@@ -250,6 +256,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
     p.act = e.activation;
     p.group_kb = group_size / tg::kBK;
     p.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : 2000);
+    p.debug_flags = o.debug_flags;
     p.err = err;
     p.c = static_cast<__half*>(C);
     p.ldc = ldc;
@@ -261,8 +268,8 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
     p.ldr = e.residual ? e.ldr : 0;
     int clusters = std::min<int64_t>(p.units, pair_clusters);
     if (o.max_ctas > 0) clusters = std::min(clusters, std::max(1, o.max_ctas / 2));
-    const cudaError_t ce = launch_w4_pair(ta, tq, ts, tc, p, 2 * clusters, stream);
-    return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+    const cudaError_t ce = launch_w4_pair<FMT>(ta, tq, ts, tc, p, 2 * clusters, stream);
+    return ce == cudaSuccess ? TG_OK : tg::record_cuda_error(ce);
   }
 
   const int64_t tiles_m = cdiv(M, tg::kBM);
@@ -285,7 +292,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
       encode(enc, &tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C,
              uint64_t(std::max<int64_t>(N & ~int64_t{7}, 8)), uint64_t(M), uint64_t(ldc) * 2, 64,
              32, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-    return TG_ERR_CUDA;
+    return tg::record_cuda_error(cudaErrorInvalidValue);
 
   tg::GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -299,6 +306,7 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
   p.act = e.activation;
   p.group_kb = group_size / tg::kBK;
   p.timeout_ns = 1000000ull * static_cast<unsigned long long>(o.timeout_ms > 0 ? o.timeout_ms : 2000);
+  p.debug_flags = o.debug_flags;
   p.err = err;
   p.c = static_cast<__half*>(C);
   p.ldc = ldc;
@@ -309,7 +317,27 @@ extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void
   p.residual = static_cast<const __half*>(e.residual);
   p.ldr = e.residual ? e.ldr : 0;
   const int grid = static_cast<int>(std::min<int64_t>(units, grid_cap));
-  const cudaError_t ce = bn == 256 ? launch_w4<256>(ta, tq, ts, tc, p, grid, stream)
-                                   : launch_w4<128>(ta, tq, ts, tc, p, grid, stream);
-  return ce == cudaSuccess ? TG_OK : TG_ERR_CUDA;
+  const cudaError_t ce = bn == 256 ? launch_w4<256, FMT>(ta, tq, ts, tc, p, grid, stream)
+                                   : launch_w4<128, FMT>(ta, tq, ts, tc, p, grid, stream);
+  return ce == cudaSuccess ? TG_OK : tg::record_cuda_error(ce);
+}
+
+}  // namespace
+
+extern "C" tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales,
+                                       void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                       int64_t ldq, int64_t lds, int64_t ldc, int group_size,
+                                       const tg_epilogue* epi, const tg_options* opt,
+                                       tg_stream_t stream) {
+  return run_dequant<tg::kFmtInt4>(A, Wq, scales, C, M, N, K, lda, ldq, lds, ldc, group_size,
+                                   epi, opt, stream);
+}
+
+extern "C" tg_status tg_gemm_nf4a16_f16(const void* A, const void* Wq, const void* scales,
+                                        void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                        int64_t ldq, int64_t lds, int64_t ldc, int group_size,
+                                        const tg_epilogue* epi, const tg_options* opt,
+                                        tg_stream_t stream) {
+  return run_dequant<tg::kFmtNf4>(A, Wq, scales, C, M, N, K, lda, ldq, lds, ldc, group_size,
+                                  epi, opt, stream);
 }

@@ -18,6 +18,11 @@
 //              tile the MMA expects; then fence.proxy.async and arrive on deq_full.
 // TMA zero fill makes the tails safe: scales past N or past the last group are 0, so those
 // weights decode to 0 whatever their nibbles.
+//
+// Every kernel here is a template over the weight format FMT: kFmtInt4 above, or kFmtNf4, the
+// W_NF4 / A_FP16 case of the same page: the same packing, with each nibble indexing the 16
+// NF4 code values of QLoRA (Dettmers et al., NeurIPS 2023, Appendix E) held in fp16,
+// w[k][n] = fp16(code16[q] * s[k/G][n]), one rounding of the exact fp16 x fp16 product.
 #pragma once
 
 #include "tg_gemm_kernel.cuh"
@@ -49,6 +54,63 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return __byte_perm(a, b, sel);
 }
 
+enum : int { kFmtInt4 = 0, kFmtNf4 = 1 };
+
+// PTX prmt.b32 in its default mode: result byte i is byte (c >> 4i) & 7 of {b, a} (a holds
+// bytes 0-3); when bit 3 of that selector nibble is set, the byte's sign bit is replicated
+// into all eight bits instead.
+__device__ __forceinline__ uint32_t prmt_ptx(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// The 16 NF4 code values (QLoRA, Appendix E) rounded to fp16, split into their low and high
+// bytes: byte e of kNf4Lo<j> is the low byte of code 4j + e.  Codes in order:
+// -1, -0.6962, -0.5251, -0.3949, -0.2844, -0.1848, -0.09105, 0, 0.07958, 0.1609, 0.2461,
+// 0.3379, 0.4407, 0.5626, 0.7230, 1 = fp16 0xbc00 0xb992 0xb833 0xb652 0xb48d 0xb1ea 0xadd4
+// 0x0000 0x2d18 0x3126 0x33e0 0x3568 0x370d 0x3880 0x39c9 0x3c00.
+constexpr uint32_t kNf4Lo0 = 0x52339200u, kNf4Lo1 = 0x00d4ea8du;
+constexpr uint32_t kNf4Lo2 = 0x68e02618u, kNf4Lo3 = 0x00c9800du;
+constexpr uint32_t kNf4Hi0 = 0xb6b8b9bcu, kNf4Hi1 = 0x00adb1b4u;
+constexpr uint32_t kNf4Hi2 = 0x3533312du, kNf4Hi3 = 0x3c393837u;
+
+// Four 16-entry byte lookups at once: byte i of the result is byte q_i of the table
+// {t0, t1, t2, t3}, with sel holding (q_i & 7) in nibble i and hi8 0xFF in byte i where q_i >= 8.
+__device__ __forceinline__ uint32_t lut16x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3,
+                                            uint32_t sel, uint32_t hi8) {
+  const uint32_t lo = prmt_ptx(t0, t1, sel);
+  const uint32_t hi = prmt_ptx(t2, t3, sel);
+  return (lo & ~hi8) | (hi & hi8);
+}
+
+// Eight NF4 weights of one packed word, in column order: pr[j] holds columns (2j, 2j+1);
+// sv holds the eight columns' fp16 scales in the same order.
+__device__ __forceinline__ uint4 dequant8_nf4(uint32_t w, const uint4& sv) {
+  const uint32_t sel_lo = w & 0x7777u;          // q0..q3 (low 3 bits)
+  const uint32_t sel_hi = (w >> 16) & 0x7777u;  // q4..q7
+  // byte i of hi8_lo is 0xFF when bit 3 of q_i is set: bits 3, 11 sit at the sign bits of
+  // the bytes of w << 4, bits 7, 15 at those of w (likewise bits 19..31 for q4..q7)
+  const uint32_t w4 = w << 4;
+  const uint32_t hi8_lo = prmt_ptx(w4, w, 0xD9C8u);
+  const uint32_t hi8_hi = prmt_ptx(w4, w, 0xFBEAu);
+  const uint32_t l03 = lut16x4(kNf4Lo0, kNf4Lo1, kNf4Lo2, kNf4Lo3, sel_lo, hi8_lo);
+  const uint32_t h03 = lut16x4(kNf4Hi0, kNf4Hi1, kNf4Hi2, kNf4Hi3, sel_lo, hi8_lo);
+  const uint32_t l47 = lut16x4(kNf4Lo0, kNf4Lo1, kNf4Lo2, kNf4Lo3, sel_hi, hi8_hi);
+  const uint32_t h47 = lut16x4(kNf4Hi0, kNf4Hi1, kNf4Hi2, kNf4Hi3, sel_hi, hi8_hi);
+  uint32_t c[4] = {prmt_ptx(l03, h03, 0x5140u), prmt_ptx(l03, h03, 0x7362u),
+                   prmt_ptx(l47, h47, 0x5140u), prmt_ptx(l47, h47, 0x7362u)};
+  const uint32_t s[4] = {sv.x, sv.y, sv.z, sv.w};
+  uint32_t pr[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __half2 h = __hmul2(*reinterpret_cast<const __half2*>(&c[j]),
+                        *reinterpret_cast<const __half2*>(&s[j]));  // one rounding
+    pr[j] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(pr[0], pr[1], pr[2], pr[3]);
+}
+
 // Eight weights of one packed word; sp[e] holds the scales of columns (e, e+4).  Returns the
 // fp16 weights in the column order 0,4,1,5,2,6,3,7, two per 32-bit word: the order in which
 // the nibble pairs come out.  The kernels store the decoded tile in that order and undo it in
@@ -72,10 +134,41 @@ __device__ __forceinline__ int perm8_column(int l) {
   return (l & ~7) + ((l & 1) << 2) + ((l & 7) >> 1);
 }
 
+// The decoded tile of format FMT stores its columns permuted (int4) or in order (NF4).
+template <int FMT>
+__device__ __forceinline__ int decoded_column(int l) {
+  return FMT == kFmtInt4 ? perm8_column(l) : l;
+}
+
+// Per-stage scale operands of a dequantiser thread from its eight columns' scales sv.
+template <int FMT>
+__device__ __forceinline__ void scale_pairs(const uint4& sv, uint32_t (&sp)[4]) {
+  if constexpr (FMT == kFmtInt4) {
+    sp[0] = prmt(sv.x, sv.z, 0x5410);  // columns (0, 4), as dequant8 pairs them
+    sp[1] = prmt(sv.x, sv.z, 0x7632);
+    sp[2] = prmt(sv.y, sv.w, 0x5410);
+    sp[3] = prmt(sv.y, sv.w, 0x7632);
+  } else {
+    sp[0] = sv.x;
+    sp[1] = sv.y;
+    sp[2] = sv.z;
+    sp[3] = sv.w;
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ uint4 decode8(uint32_t w, const uint32_t (&sp)[4]) {
+  if constexpr (FMT == kFmtInt4) {
+    return dequant8(w, sp);
+  } else {
+    return dequant8_nf4(w, make_uint4(sp[0], sp[1], sp[2], sp[3]));
+  }
+}
+
 // tmA: fp16 A {K, M} box {64, 128} SW128; tmQ: uint32 Wq {ceil(N/8), K} box {BN/8, 64};
 // tmS: fp16 scales {N, ceil(K/G)} box {BN, 1}; tmOut: fp16 C {n_tma, M} box {64, 32} SW128.
 // p.splits must be 1; p.kb_per_split = p.num_kb; p.group_kb = G / 64.
-template <int BN>
+template <int BN, int FMT>
 __global__ void __launch_bounds__(kW4Threads, 1)
     tg_gemm_w4_kernel(const __grid_constant__ CUtensorMap tmA,
                       const __grid_constant__ CUtensorMap tmQ,
@@ -141,6 +234,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
+      bool dropped = false;
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
         // scale row of k-block kb: g = kb / group_kb, advanced with a counter (one division
@@ -150,17 +244,21 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto w4_producer_done;
-          const uint32_t fb = smem_u32(&load_full[stage]);
-          mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-          tma_load_2d(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, w.m_blk * kBM);
-          tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
-          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * BN, g);
+          if ((p.debug_flags & kDebugDropFirstStage) && blockIdx.x == 0 && !dropped) {
+            dropped = true;  // injected fault: this stage is never filled
+          } else {
+            const uint32_t fb = smem_u32(&load_full[stage]);
+            mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+            tma_load_2d(smem_u32(sA + stage * Cfg::kAStage), &tmA, fb, kb * kBK, w.m_blk * kBM);
+            tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
+            tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * BN, g);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
           if (++g_rem == p.group_kb) {
             g_rem = 0;
             ++g;
           }
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -229,8 +327,9 @@ __global__ void __launch_bounds__(kW4Threads, 1)
       tc_fence_after();
       const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * Cfg::kAccStride);
-      epilogue_tile<BN, false, true>(&tmOut, p, tl, w.m_blk * kBM + q * 32, w.n_blk * BN, 0,
-                                     stg, sb, smem_u32(&tempty[buf]), false, lane);
+      epilogue_tile<BN, false, FMT == kFmtInt4>(&tmOut, p, tl, w.m_blk * kBM + q * 32,
+                                                w.n_blk * BN, 0, stg, sb,
+                                                smem_u32(&tempty[buf]), false, lane);
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
@@ -257,8 +356,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         }
         // the eight scales of this thread's columns, paired (e, e+4) like dequant8's halves
         const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
-        const uint32_t sp[4] = {prmt(sv.x, sv.z, 0x5410), prmt(sv.x, sv.z, 0x7632),
-                                prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
+        uint32_t sp[4];
+        scale_pairs<FMT>(sv, sp);
         const uint32_t* q = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
         uint8_t* bdst = sB + stage * Cfg::kBStage + box * 8192;
         // all of this thread's words first, then independent decodes: the rows give the
@@ -270,7 +369,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
           const int r = row_first + i * kRowStep;
-          const uint4 v = dequant8(words[i], sp);
+          const uint4 v = decode8<FMT>(words[i], sp);
           *reinterpret_cast<uint4*>(bdst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
         }
         fence_async_smem();
@@ -341,6 +440,7 @@ struct W4PairCfg {
 // tmA: fp16 A {K, M} box {64, 128} SW128; tmQ: uint32 Wq {ceil(N/8), K} box {16, 64};
 // tmS: fp16 scales {N, ceil(K/G)} box {128, 1}; tmOut: fp16 C {n_tma, M} box {64, 32} SW128.
 // p.tiles_m / p.tiles_n count 256 x 256 pair tiles; p.splits == 1; p.group_kb = G / 64.
+template <int FMT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads, 1)
     tg_gemm_w4_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmQ,
@@ -435,6 +535,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;      // the leader's full barriers
       uint32_t qarmed = 0, qarmed_parity = 0;    // this CTA's qfull barriers
+      bool dropped = false;
       const uint32_t full0_leader = mapa_shared(smem_u32(&full[0]), 0);
       for (int u = cluster; u < p.units; u += nclusters) {
         const Unit w = unit_of(p, u);
@@ -445,19 +546,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto w4pair_producer_done;
-          if (rank == 0) {
-            mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * Cfg::kAStage);
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if ((p.debug_flags & kDebugDropFirstStage) && cluster == 0 && rank == 0 && !dropped) {
+            dropped = true;  // injected fault: the leader neither arms nor fills this stage
+          } else {
+            if (rank == 0) {
+              mbar_arrive_expect_tx(smem_u32(&full[stage]), 2 * Cfg::kAStage);
+              armed |= 1u << stage;
+              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            }
+            tma_load_2d_pair(smem_u32(sA + stage * Cfg::kAStage), &tmA,
+                             full0_leader + 8u * stage, kb * kBK, arow);
+            const uint32_t qb = smem_u32(&qfull[stage]);
+            mbar_arrive_expect_tx(qb, Cfg::kQTx);
+            tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, qb, bcol / 8, kb * kBK);
+            tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, qb, bcol, g);
+            qarmed |= 1u << stage;
+            qarmed_parity = (qarmed_parity & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d_pair(smem_u32(sA + stage * Cfg::kAStage), &tmA, full0_leader + 8u * stage,
-                           kb * kBK, arow);
-          const uint32_t qb = smem_u32(&qfull[stage]);
-          mbar_arrive_expect_tx(qb, Cfg::kQTx);
-          tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, qb, bcol / 8, kb * kBK);
-          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, qb, bcol, g);
-          qarmed |= 1u << stage;
-          qarmed_parity = (qarmed_parity & ~(1u << stage)) | (phase << stage);
           if (++g_rem == p.group_kb) {
             g_rem = 0;
             ++g;
@@ -540,8 +645,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
                           static_cast<uint32_t>(buf * Cfg::kAccStride);
       const int row0 = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM + q * 32;
       const uint32_t release_bar = mapa_shared(smem_u32(&tempty[buf]), 0);
-      epilogue_tile<Cfg::kBN, false, true>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN, 0, stg,
-                                           sb, release_bar, true, lane);
+      epilogue_tile<Cfg::kBN, false, FMT == kFmtInt4>(&tmOut, p, tl, row0, w.n_blk * Cfg::kBN,
+                                                      0, stg, sb, release_bar, true, lane);
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
@@ -568,8 +673,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
           break;
         }
         const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
-        const uint32_t sp[4] = {prmt(sv.x, sv.z, 0x5410), prmt(sv.x, sv.z, 0x7632),
-                                prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
+        uint32_t sp[4];
+        scale_pairs<FMT>(sv, sp);
         const uint32_t* qw = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
         uint8_t* bdst = sB + stage * Cfg::kBStage + box * 8192;
         constexpr int kRows = 64 / kRowStep;
@@ -579,7 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(W4PairCfg::kThreads,
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
           const int r = row_first + i * kRowStep;
-          const uint4 v = dequant8(words[i], sp);
+          const uint4 v = decode8<FMT>(words[i], sp);
           *reinterpret_cast<uint4*>(bdst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
         }
         fence_async_smem();
@@ -649,7 +754,7 @@ struct W4TCfg {
 // p.tiles_n counts 128-column blocks of C.  p.splits == 1.  With p.tail, units [0, n_full)
 // are whole tiles and each later tile is two units, one per K half (see unit_of); tail_ws
 // holds 2 x 4 x 32 x BMT floats per split tile and tail_cnt 4 zeroed counters per split tile.
-template <int BMT>
+template <int BMT, int FMT>
 __global__ void __launch_bounds__(kW4TThreads, 1)
     tg_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmQ,
@@ -712,6 +817,7 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, armed_parity = 0;
+      bool dropped = false;
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const Unit w = unit_of(p, u);
         // scale row of k-block kb: g = kb / group_kb, advanced with a counter (one division
@@ -721,17 +827,22 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
         for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto w4t_producer_done;
-          const uint32_t fb = smem_u32(&load_full[stage]);
-          mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
-          tma_load_2d(smem_u32(sAct + stage * Cfg::kActStage), &tmA, fb, kb * kBK, w.m_blk * BMT);
-          tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
-          tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * Cfg::kNTile, g);
+          if ((p.debug_flags & kDebugDropFirstStage) && blockIdx.x == 0 && !dropped) {
+            dropped = true;  // injected fault: this stage is never filled
+          } else {
+            const uint32_t fb = smem_u32(&load_full[stage]);
+            mbar_arrive_expect_tx(fb, Cfg::kTxBytes);
+            tma_load_2d(smem_u32(sAct + stage * Cfg::kActStage), &tmA, fb, kb * kBK,
+                        w.m_blk * BMT);
+            tma_load_2d(smem_u32(sQ + stage * Cfg::kQStage), &tmQ, fb, w.n_blk * W, kb * kBK);
+            tma_load_2d(smem_u32(sS + stage * Cfg::kSStage), &tmS, fb, w.n_blk * Cfg::kNTile, g);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
           if (++g_rem == p.group_kb) {
             g_rem = 0;
             ++g;
           }
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
@@ -826,7 +937,7 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           tmem_wait_ld(r);
         }
       };
-      const int n = w.n_blk * Cfg::kNTile + perm8_column(q * 32 + lane);  // TMEM lane -> column
+      const int n = w.n_blk * Cfg::kNTile + decoded_column<FMT>(q * 32 + lane);  // TMEM lane -> column
       const int m_base = w.m_blk * BMT;
       const bool n_ok = n < p.N;
       const float bias = (n_ok && p.bias) ? __half2float(p.bias[n]) : 0.0f;
@@ -930,8 +1041,8 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           break;
         }
         const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
-        const uint32_t sp[4] = {prmt(sv.x, sv.z, 0x5410), prmt(sv.x, sv.z, 0x7632),
-                                prmt(sv.y, sv.w, 0x5410), prmt(sv.y, sv.w, 0x7632)};
+        uint32_t sp[4];
+        scale_pairs<FMT>(sv, sp);
         const uint32_t* qw = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
         uint8_t* ddst = sDec + stage * Cfg::kDecStage + box * 8192;
         constexpr int kRows = 64 / kRowStep;
@@ -941,7 +1052,7 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
           const int r = row_first + i * kRowStep;
-          const uint4 v = dequant8(words[i], sp);
+          const uint4 v = decode8<FMT>(words[i], sp);
           *reinterpret_cast<uint4*>(ddst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
         }
         fence_async_smem();

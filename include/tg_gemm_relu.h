@@ -26,7 +26,8 @@
  *  - Device support: compute capability 10.3 (GB300) only (TG_ERR_UNSUPPORTED_DEVICE).
  *  - Thread safety: every entry point may be called from several host threads at once.
  *  - CUDA graphs: the asynchronous device-pointer entry points (tg_gemm_relu_f16, _ex,
- *    tg_gemm_f16_epilogue, tg_gemm_f16_t, tg_relu_backward_f16, tg_gemm_w4a16_f16) may be
+ *    tg_gemm_f16_epilogue, tg_gemm_f16_t, tg_relu_backward_f16, tg_gemm_w4a16_f16,
+ *    tg_gemm_nf4a16_f16) may be
  *    captured by stream capture once the calling thread has made one eager call on the device
  *    (that first call sets up library state); scratch is taken stream-ordered from the
  *    library's pool and becomes graph allocation nodes.  tg_gemm_relu_f16_host synchronises
@@ -107,7 +108,8 @@ typedef struct {
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
  * arrival), so the consumer's wait on that stage runs out; the kernel records the timeout,
- * drains and returns.  Only for the error-path test. */
+ * drains and returns.  Honoured by every GEMM kernel (fp16, int4 and NF4 weights).  Only for
+ * the error-path test. */
 #define TG_DEBUG_DROP_FIRST_STAGE 1
 
 /* What a call will do; filled by tg_plan_query (host only, no device needed). */
@@ -196,6 +198,21 @@ tg_status tg_gemm_w4a16_f16(const void* A, const void* Wq, const void* scales, v
                             int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldq,
                             int64_t lds, int64_t ldc, int group_size, const tg_epilogue* epi,
                             const tg_options* opt, tg_stream_t stream);
+
+/*
+ * Dequantising GEMM with 4-bit NormalFloat (NF4) weights and fp16 activations (the W_NF4 /
+ * A_FP16 case of the TileLang paper-reading page, section 5):
+ *     C = fp16( epilogue( A · W ) ),   W[k][n] = fp16( code16[q[k][n]] * scales[k / G][n] )
+ * code16[q] is the NF4 code value q of QLoRA (Dettmers et al., NeurIPS 2023, Appendix E:
+ * sixteen quantiles of a standard normal scaled to [-1, 1], with an exact 0 at q = 7) rounded
+ * to fp16; the product of two fp16 values is rounded to fp16 once.  Packing of Wq, the
+ * scales, every other argument, the kernels chosen, the options, alignment and errors are
+ * those of tg_gemm_w4a16_f16.
+ */
+tg_status tg_gemm_nf4a16_f16(const void* A, const void* Wq, const void* scales, void* C,
+                             int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldq,
+                             int64_t lds, int64_t ldc, int group_size, const tg_epilogue* epi,
+                             const tg_options* opt, tg_stream_t stream);
 
 /*
  * The plan tg_gemm_relu_f16_ex would use for these arguments on a device with num_sms SMs.

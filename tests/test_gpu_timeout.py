@@ -57,3 +57,39 @@ def test_host_entry_reports_clean_status():
     st = binding.tg_gemm_relu_f16_host(a.ctypes.data, b.ctypes.data, out.ctypes.data, M, N, K,
                                        K, N, N, 1, 0)
     assert st == binding.TG_OK
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nf4"])
+@pytest.mark.parametrize("kernel", ["swapped", "single_cta", "cta_pair"])
+def test_dequant_kernels_dropped_stage_times_out(fmt, kernel):
+    # the same injected fault in the three dequantising GEMM kernels: their waits are bounded
+    # like the fp16 kernels'; after the timeout the next call on the context is correct
+    from fp16_gemm_relu_gb300 import build
+
+    from tests.test_gpu_w4 import check, make, run_w4
+
+    build.build()
+    torch.cuda.set_device(0)
+    binding.tg_device_error_check(clear=True)
+    M, N, K, G = 256, 512, 2048, 128
+    a, Wq, S = make(M, N, K, G, 41)
+    base = {"swapped": {"swap_ab": 1}, "single_cta": {"swap_ab": -1, "block_n": 128},
+            "cta_pair": {"swap_ab": -1, "pair": 1}}[kernel]
+    opts = dict(base, debug_flags=binding.TG_DEBUG_DROP_FIRST_STAGE, timeout_ms=200)
+    fn = binding.tg_gemm_w4a16_f16 if fmt == "int4" else binding.tg_gemm_nf4a16_f16
+    A = torch.from_numpy(a).cuda()
+    Q = torch.from_numpy(Wq.view(np.int32)).cuda()
+    Sc = torch.from_numpy(S).cuda()
+    C = torch.zeros((M, N), dtype=torch.float16, device="cuda")
+    st = fn(A.data_ptr(), Q.data_ptr(), Sc.data_ptr(), C.data_ptr(), M, N, K, K, Wq.shape[1],
+            S.shape[1], N, G, 1, 0, 0, 0, opts, torch.cuda.current_stream().cuda_stream)
+    assert st == binding.TG_OK  # queued; the failure is only visible after it ran
+    st, word = binding.tg_device_error_check(clear=True)
+    assert st == binding.TG_ERR_TIMEOUT, (st, hex(word))
+    assert word & 1 and ((word >> 8) & 0xFF) in (1, 2, 3)
+    st, word = binding.tg_device_error_check(clear=False)
+    assert st == binding.TG_OK and word == 0
+    got = run_w4(a, Wq, S, N, G, act=1, options=base, fmt=fmt)
+    check(got, a, Wq, S, N, G, "relu", fmt=fmt)
+    st, word = binding.tg_device_error_check(clear=True)
+    assert st == binding.TG_OK and word == 0

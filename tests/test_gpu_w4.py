@@ -28,16 +28,18 @@ def _built():
     assert st == binding.TG_OK, f"device error word {word:#x}"
 
 
-def run_w4(a, Wq, S, N, G, act=0, bias=None, residual=None, options=None):
+def run_w4(a, Wq, S, N, G, act=0, bias=None, residual=None, options=None, fmt="int4"):
     M, K = a.shape
     A = torch.from_numpy(inputs.embed(a, -(-K // 8) * 8)).cuda()
-    Q = torch.from_numpy(Wq.view(np.int32)).cuda()
-    Sc = torch.from_numpy(S).cuda()
+    # row-major buffers whatever the caller's array layout (the ABI reads ldq / lds strides)
+    Q = torch.from_numpy(np.ascontiguousarray(Wq).view(np.int32)).cuda()
+    Sc = torch.from_numpy(np.ascontiguousarray(S)).cuda()
     ldc = -(-N // 8) * 8
     C = torch.full((M, ldc), float("nan"), dtype=torch.float16, device="cuda")
     b = torch.from_numpy(bias).cuda() if bias is not None else None
     r = torch.from_numpy(residual).cuda() if residual is not None else None
-    st = binding.tg_gemm_w4a16_f16(A.data_ptr(), Q.data_ptr(), Sc.data_ptr(), C.data_ptr(), M, N,
+    fn = binding.tg_gemm_w4a16_f16 if fmt == "int4" else binding.tg_gemm_nf4a16_f16
+    st = fn(A.data_ptr(), Q.data_ptr(), Sc.data_ptr(), C.data_ptr(), M, N,
                                    K, A.shape[1], Wq.shape[1], S.shape[1], ldc, G, act,
                                    b.data_ptr() if b is not None else 0,
                                    r.data_ptr() if r is not None else 0,
@@ -58,9 +60,10 @@ def make(M, N, K, G, seed, scale=None):
     return a, Wq, S
 
 
-def check(got, a, Wq, S, N, G, act="none", bias=None, residual=None, rows=None, cols=None):
+def check(got, a, Wq, S, N, G, act="none", bias=None, residual=None, rows=None, cols=None,
+          fmt="int4"):
     K = a.shape[1]
-    w = oracle.dequant_w4(Wq, S, K, N, G)
+    w = (oracle.dequant_w4 if fmt == "int4" else oracle.dequant_nf4)(Wq, S, K, N, G)
     r = oracle.gemm_epilogue(a, w, act, bias=bias, residual=residual, rows=rows, cols=cols)
     ref = {"out16_f64acc": r["out16_f64acc"], "acc_f64": r["pre_f64"]}
     zr = act == "relu" and residual is None
