@@ -135,14 +135,20 @@ struct Plan {
   int64_t lda_p, ldb_p, ldw;     // leading dimensions of the scratch copies / workspace
   int64_t off_a, off_b, off_w;   // byte offsets inside the scratch block
   int64_t off_tail_ws, off_tail_cnt, tail_cnt_bytes;  // tail-split partials and counters
+  // A read by row classes: rows per class (a multiple of the 256-row pair tile), each class's
+  // element shift past a 32-byte boundary, and the first-window copy's offset in scratch
+  int64_t cls_rows, off_first;
+  int cls_shift[tg::kARowClasses];
 };
 
 // Per-k-block cost in SM cycles of an output tile 128 x bn: the tensor-core time (a
 // 128 x bn x 16 MMA takes bn/8 cycles, four per k-block) or the time to bring the stage's
-// bytes in from L2 at ~96 B/cycle, whichever is longer.
+// bytes in from L2, whichever is longer.  The L2 feed rate, ~87 B/cycle per SM, is what the
+// 128 x 256 tile sustains on 8192^3 (~1630 TFLOP/s, ~10% below the CTA-pair tile, whose
+// 32 KB per SM and k-block stay within it: the pair's 512 cycles below).
 double kblock_cycles(int bn) {
   const double mma = 2.0 * bn;
-  const double load = (16384.0 + 128.0 * bn) / 96.0;
+  const double load = (16384.0 + 128.0 * bn) / 87.0;
   return std::max(mma, load);
 }
 
@@ -160,7 +166,7 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 192 && o.block_n != 256)
     return TG_ERR_INVALID_ARG;
   if (o.split_k < 0 || o.panel_m < 0 || o.max_ctas < 0 || o.timeout_ms < 0 || o.pair < -1 ||
-      o.pair > 1 || o.tail < -1 || o.tail > 1)
+      o.pair > 1 || o.tail < -1 || o.tail > 1 || o.a_in_place < 0 || o.a_in_place > 1)
     return TG_ERR_INVALID_ARG;
   if (o.pair == 1 && o.block_n != 0 && o.block_n != 256) return TG_ERR_INVALID_ARG;
 
@@ -262,6 +268,39 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
                      : static_cast<int>(std::min<int64_t>(P.units, grid_cap));
   P.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : kDefaultPanel, P.tiles_m));
   P.workspace_epilogue = (P.split_k > 1 || !c_direct) ? 1 : 0;
+  // On request (tg_options.a_in_place), an A whose rows TMA cannot describe (lda not a
+  // multiple of 8) is read in place through 16 row classes (AClassMaps) instead of being
+  // copied, when A itself is 32-byte aligned, the plan uses CTA pairs on the forward layout and
+  // the class-major row order adds at most 3% of M tiles.  The partial sums then go through the
+  // float32 workspace in class-major row order and the reduction writes them back to C's rows.
+  // Each class's K windows start up to 15 elements early, which can add one k-block.  It saves
+  // the copy's scratch, but is not the default: a class's rows lie 32 lda bytes apart, so
+  // three in four start inside a 128-byte line and every box row spans two lines, which on
+  // 4095 x 3073 x 65537 made the GEMM 29% slower (1226 against 952 us) than on the aligned copy.
+  if (o.a_in_place > 0 && P.repack_a && !o.force_repack && !ta && !tb && P.cta_pair &&
+      lda % 8 != 0 && a % 32 == 0 && K >= tg::kBK && M >= 2 * tg::kBM) {
+    const int64_t rows = round_up(cdiv(M, tg::kARowClasses), 2 * tg::kBM);
+    const int64_t tiles_cls = tg::kARowClasses * rows / (2 * tg::kBM);
+    if (tiles_cls * 100 <= P.tiles_m * 103) {
+      int emax = 0;
+      for (int r = 0; r < tg::kARowClasses; ++r) {
+        pl.cls_shift[r] = static_cast<int>((int64_t(r) * lda) % tg::kARowClasses);
+        emax = std::max(emax, pl.cls_shift[r]);
+      }
+      pl.cls_rows = rows;
+      P.a_row_classes = tg::kARowClasses;
+      P.repack_a = 0;
+      P.workspace_epilogue = 1;
+      P.kblocks = cdiv(K + emax, tg::kBK);
+      P.kblocks_per_split = cdiv(P.kblocks, P.split_k);
+      P.split_k = static_cast<int>(cdiv(P.kblocks, P.kblocks_per_split));
+      P.tiles_m = tiles_cls;
+      P.units = P.tiles_m * P.tiles_n * P.split_k;
+      if (P.units >= (int64_t{1} << 31)) return TG_ERR_INVALID_ARG;
+      P.grid = 2 * static_cast<int>(std::min<int64_t>(P.units, pair_cap));
+      P.panel_m = static_cast<int>(std::min<int64_t>(o.panel_m ? o.panel_m : kDefaultPanel, P.tiles_m));
+    }
+  }
   // Tail split (tg_options.tail: 0 chooses, 1 forces, -1 never): when the last wave of pair
   // tiles would leave more than half the clusters idle, its r tiles run as 2r K halves
   // instead.  On 8192^3 (36 tiles left for 76 clusters) launches interleaved with whole-tile
@@ -290,10 +329,15 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
     pl.off_b = off;
     off += round_up((tb ? N : K) * pl.ldb_p * 2, 256);
   }
+  if (P.a_row_classes) {  // the first 64-k window of every class-major row, pre-shifted
+    pl.off_first = off;
+    off += round_up(P.a_row_classes * pl.cls_rows * tg::kBK * 2, 256);
+  }
   if (P.workspace_epilogue) {
     pl.ldw = round_up(N, 32);  // 128-byte rows for the same reason
     pl.off_w = off;
-    off += round_up(int64_t(P.split_k) * M * pl.ldw * 4, 256);
+    const int64_t ws_rows = P.a_row_classes ? P.a_row_classes * pl.cls_rows : M;
+    off += round_up(int64_t(P.split_k) * ws_rows * pl.ldw * 4, 256);
   }
   if (P.tail_tiles) {
     pl.off_tail_ws = off;
@@ -303,7 +347,7 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
     off += pl.tail_cnt_bytes;
   }
   P.workspace_bytes = off;
-  P.kernels = 1 + P.repack_a + P.repack_b + P.workspace_epilogue;
+  P.kernels = 1 + P.repack_a + P.repack_b + P.workspace_epilogue + (P.a_row_classes ? 1 : 0);
   *out = pl;
   return TG_OK;
 }
@@ -355,13 +399,39 @@ __global__ void tg_pack_rows_kernel(const uint16_t* __restrict__ src, int64_t ld
   }
 }
 
+// Element shifts of the 16 row classes of A (AClassMaps), passed by value.
+struct ClassShifts {
+  int e[tg::kARowClasses];
+};
+
+// The first 64-k window of every row of A in class-major order, shifted like the class's
+// windows: F[(r * cls_rows + j) * 64 + t] = A[16 j + r][t - e_r] where 0 <= t - e_r < K and
+// 16 j + r < M, else +0 (so the window's elements before k = 0 are zero).
+__global__ void tg_first_window_kernel(const uint16_t* __restrict__ A, int64_t lda, int64_t M,
+                                       int64_t K, int64_t cls_rows, ClassShifts sh,
+                                       uint16_t* __restrict__ F) {
+  const int64_t total = tg::kARowClasses * cls_rows * tg::kBK;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t row = idx / tg::kBK;
+    const int t = static_cast<int>(idx - row * tg::kBK);
+    const int r = static_cast<int>(row / cls_rows);
+    const int64_t i = (row - r * cls_rows) * tg::kARowClasses + r;
+    const int64_t k = t - sh.e[r];
+    F[idx] = (i < M && k >= 0 && k < K) ? A[i * lda + k] : uint16_t(0);
+  }
+}
+
 // C[i, j] = fp16(epilogue(sum_{s=0}^{splits-1} W[s][i][j])), the splits added in increasing s
 // (deterministic), then the same fused epilogue as the GEMM kernel (bias, activation,
 // residual).  W rows are ldw floats (multiple of 4, 16-byte aligned); C may have any 2-byte
 // alignment and leading dimension.  p supplies act, bias, residual, ldr, M and N.
+// With cls_rows > 0 the workspace rows are in class-major order (A read by row classes): row i
+// of C is workspace row (i mod 16) * cls_rows + i / 16.
 __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ldw,
                                         int64_t split_stride, int splits, __half* C,
-                                        int64_t ldc, const tg::GemmParams p) {
+                                        int64_t ldc, const tg::GemmParams p,
+                                        int64_t cls_rows) {
   const int64_t M = p.M, N = p.N;
   const int64_t cpr = (N + 3) >> 2;
   const int64_t total = M * cpr;
@@ -369,7 +439,8 @@ __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ld
        idx += int64_t(gridDim.x) * blockDim.x) {
     const int64_t r = idx / cpr;
     const int64_t c0 = (idx - r * cpr) << 2;
-    const float* w = ws + r * ldw + c0;
+    const int64_t wr = cls_rows > 0 ? (r % tg::kARowClasses) * cls_rows + r / tg::kARowClasses : r;
+    const float* w = ws + wr * ldw + c0;
     // splits == 0: the empty sum (K == 0 with a bias or residual epilogue)
     float4 acc = splits > 0 ? __ldg(reinterpret_cast<const float4*>(w)) : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 1; s < splits; ++s) {
@@ -484,7 +555,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     gp.M = static_cast<int>(M);
     gp.N = static_cast<int>(N);
     tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
-        nullptr, 0, 0, 0, static_cast<__half*>(C), ldc, gp);
+        nullptr, 0, 0, 0, static_cast<__half*>(C), ldc, gp, 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? TG_OK : cuda_fail(e);
   }
@@ -533,14 +604,40 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
   tg::GemmLaunch L;
   std::memset(&L, 0, sizeof(L));
+  // A read in place by row classes: the pre-shifted first windows, then one map per class
+  // (class r: base 2 (r lda - e_r) bytes past A, 32-byte aligned because A is and e_r =
+  // r lda mod 16; rows 32 lda bytes apart; x = k + e_r)
+  tg::AClassMaps cls;
+  std::memset(&cls, 0, sizeof(cls));
+  const int64_t ws_rows = P.a_row_classes ? P.a_row_classes * pl.cls_rows : M;
+  if (P.a_row_classes) {
+    uint16_t* first = reinterpret_cast<uint16_t*>(scratch + pl.off_first);
+    ClassShifts sh;
+    for (int r = 0; r < tg::kARowClasses; ++r) sh.e[r] = pl.cls_shift[r];
+    tg_first_window_kernel<<<aux_grid(ws_rows * tg::kBK, ds->sm_count), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(A), lda, M, K, pl.cls_rows, sh, first);
+    if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
+    CUresult cr = encode_2d(enc, &cls.first, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, first,
+                            uint64_t(tg::kBK), uint64_t(ws_rows), uint64_t(tg::kBK) * 2, tg::kBK,
+                            tg::kBM);
+    for (int r = 0; r < tg::kARowClasses && cr == CUDA_SUCCESS; ++r) {
+      const int64_t rows_r = (M - r + tg::kARowClasses - 1) / tg::kARowClasses;  // M >= 256 > r
+      const uint16_t* base = static_cast<const uint16_t*>(A) + (int64_t(r) * lda - pl.cls_shift[r]);
+      cr = encode_2d(enc, &cls.cls[r], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base,
+                     uint64_t(K + pl.cls_shift[r]), uint64_t(rows_r),
+                     uint64_t(lda) * 2 * tg::kARowClasses, tg::kBK, tg::kBM);
+    }
+    if (cr != CUDA_SUCCESS) return fail(cuda_fail(cudaErrorInvalidValue));
+  }
   // A: K-major box {64 K, 128 rows} or, stored K x M, two MN-major boxes {64 M, 64 K};
   // B: MN-major boxes {64 N, 64 K} or, stored N x K, one K-major box {64 K, BN (or 128) rows}
   // the CTA-pair kernel stages 128 k: its MN-major boxes are {64, 128 K}
   const uint32_t mn_box_k = P.cta_pair ? uint32_t(tg::PairCfgFwd::kKB * tg::kBK) : tg::kBK;
-  CUresult cr = ta ? encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(M),
-                               uint64_t(K), uint64_t(lda_e) * 2, 64, mn_box_k)
-                   : encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(K),
-                               uint64_t(M), uint64_t(lda_e) * 2, tg::kBK, tg::kBM);
+  CUresult cr = P.a_row_classes ? CUDA_SUCCESS  // A comes through cls
+                : ta ? encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(M),
+                                 uint64_t(K), uint64_t(lda_e) * 2, 64, mn_box_k)
+                     : encode_2d(enc, &L.a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ae, uint64_t(K),
+                                 uint64_t(M), uint64_t(lda_e) * 2, tg::kBK, tg::kBM);
   if (cr == CUDA_SUCCESS)
     cr = tb ? encode_2d(enc, &L.b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Be, uint64_t(K), uint64_t(N),
                         uint64_t(ldb_e) * 2, tg::kBK, P.cta_pair ? 128u : uint32_t(P.block_n))
@@ -549,7 +646,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   float* ws = P.workspace_epilogue ? reinterpret_cast<float*>(scratch + pl.off_w) : nullptr;
   if (cr == CUDA_SUCCESS) {
     if (ws)
-      cr = encode_ws_3d(enc, &L.out, ws, uint64_t(N), uint64_t(M), uint64_t(P.split_k),
+      cr = encode_ws_3d(enc, &L.out, ws, uint64_t(N), uint64_t(ws_rows), uint64_t(P.split_k),
                         uint64_t(pl.ldw));
     else  // a tile store writes whole 16-byte chunks: the map stops at N rounded down to 8
       cr = encode_2d(enc, &L.out, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, C,
@@ -591,9 +688,18 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   gp.M = static_cast<int>(M);
   gp.N = static_cast<int>(N);
   gp.n_tma = static_cast<int>(N & ~int64_t{7});
+  const tg::GemmParams reduce_params = gp;  // the reduction writes C's M rows
+  if (P.a_row_classes) {
+    gp.M = static_cast<int>(ws_rows);  // the GEMM writes class-major workspace rows
+    gp.cls_tiles = static_cast<int>(pl.cls_rows / (2 * tg::kBM));
+    for (int r = 0; r < tg::kARowClasses; ++r)
+      gp.cls_shift[r] = static_cast<unsigned char>(pl.cls_shift[r]);
+  }
   L.grid = P.grid;
   L.stream = stream;
-  if (P.cta_pair) {
+  if (P.a_row_classes) {
+    e = tg::launch_gemm_pair_cls(cls, L);
+  } else if (P.cta_pair) {
     e = tg::launch_gemm_pair(L, ws != nullptr);
   } else switch (P.block_n) {
     case 256: e = tg::launch_gemm_bn256(L, ws != nullptr); break;
@@ -604,7 +710,8 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
 
   if (ws) {
     tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
-        ws, pl.ldw, int64_t(M) * pl.ldw, P.split_k, static_cast<__half*>(C), ldc, gp);
+        ws, pl.ldw, ws_rows * pl.ldw, P.split_k, static_cast<__half*>(C), ldc, reduce_params,
+        P.a_row_classes ? pl.cls_rows : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
   }
   if (scratch && (e = cudaFreeAsync(scratch, stream)) != cudaSuccess) return cuda_fail(e);
@@ -707,7 +814,7 @@ cudaError_t launch_splitk_reduce(const float* ws, int64_t ldw, int64_t split_str
                                  void* C, int64_t ldc, const GemmParams& p, int num_sms,
                                  cudaStream_t stream) {
   tg_splitk_reduce_kernel<<<aux_grid(int64_t(p.M) * cdiv(p.N, 4), num_sms), 256, 0, stream>>>(
-      ws, ldw, split_stride, splits, static_cast<__half*>(C), ldc, p);
+      ws, ldw, split_stride, splits, static_cast<__half*>(C), ldc, p, 0);
   return cudaGetLastError();
 }
 
@@ -942,6 +1049,6 @@ tg_status tg_release_workspace(void) {
   return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }
 
-int tg_version(void) { return 100; }
+int tg_version(void) { return 200; }
 
 }  // extern "C"

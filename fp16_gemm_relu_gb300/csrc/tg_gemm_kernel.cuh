@@ -42,6 +42,8 @@ constexpr int kStagingBuf = 32 * 128;  // one epilogue warp's 32 rows x 128 byte
 constexpr int kSmemLimit = 232448;     // 227 KB opt-in dynamic shared memory per block
 constexpr int kSmemReserve = 1024 + 256;
 
+constexpr int kARowClasses = 16;  // row classes of an A read without repacking (AClassMaps)
+
 enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 enum : int { kDebugDropFirstStage = 1 };
 
@@ -78,6 +80,12 @@ struct GemmParams {
   const __half* bias;
   const __half* residual;
   long long ldr;
+  // A read by row classes (CTA-pair kernel, float32 output; see AClassMaps): M tile m holds
+  // rows 16 j + r of class r = m / cls_tiles, j from (m % cls_tiles) * 256; class r's rows
+  // start cls_shift[r] elements past a 32-byte boundary, so its K windows (and the matching B
+  // rows) start that many elements before each multiple of 64
+  int cls_tiles;
+  unsigned char cls_shift[kARowClasses];
 };
 
 enum : int { kActNone = 0, kActRelu = 1, kActGelu = 2, kActGeluTanh = 3 };
@@ -1000,15 +1008,32 @@ struct PairCfgT {
 };
 using PairCfgFwd = PairCfgT<2>;
 
+// A with a leading dimension that TMA cannot describe (lda * 2 not a multiple of 16), read in
+// place through row classes instead of being copied into aligned scratch.  Rows i = 16 j + r
+// (class r) lie 32 * lda bytes apart, a multiple of 32, so every row of a class starts at the
+// same offset from a 32-byte boundary: e_r elements past it.  Map cls[r] starts at that
+// boundary before row r (A itself 32-byte aligned), so element (16 j + r, k) sits at x = k + e_r
+// of row j: the box at x = 64 kb holds k in [64 kb - e_r, 64 kb - e_r + 64), every row of the
+// class the same window, and the B tile is loaded from K row 64 kb - e_r to match (B's K
+// coordinate has no alignment rule; rows before 0 or past K read as zero).  The first window
+// would hold e_r elements before the row's start, so it comes from `first`: a small copy of
+// each row's window [-e_r, 64 - e_r) with zeros before k = 0, in class-major row order.
+struct AClassMaps {
+  CUtensorMap cls[kARowClasses];  // fp16, dims {K + e_r, rows of class r}, row stride 32 lda bytes,
+                                  // box {64, 128}, 128B swizzle
+  CUtensorMap first;              // fp16, dims {64, 16 * class rows}, box {64, 128}, 128B swizzle
+};
+
 // Same maps as tg_gemm_tc_kernel, with the operand layouts fixed at compile time (A_MN: A stored
 // K x M; B_K: B stored N x K) and 128-k stages: MN-major operands come as {64, 128 K} boxes,
 // K-major ones as one {64 K, 128} box per 64-k block.  tiles_m/tiles_n in p count 256 x 256
-// pair tiles.
-template <bool OUT_F32, bool A_MN, bool B_K>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+// pair tiles.  With A_CLS (float32 output, forward layout) A comes through `cls` (tmA unused)
+// and M tiles index class-major rows.
+template <bool OUT_F32, bool A_MN, bool B_K, bool A_CLS>
+__device__ __forceinline__ void pair_gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                               const CUtensorMap& tmOut, const GemmParams& p,
+                                               const AClassMaps* cls) {
+  static_assert(!A_CLS || (OUT_F32 && !A_MN && !B_K), "row classes: float32 output, forward layout");
   using Cfg = PairCfgFwd;
   constexpr int S = Cfg::kStages;
   constexpr int KB = Cfg::kKB;
@@ -1048,7 +1073,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmA);
+    if constexpr (A_CLS) {
+      prefetch_tmap(&cls->first);
+    } else {
+      prefetch_tmap(&tmA);
+    }
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmOut);
   }
@@ -1072,6 +1101,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const Unit w = unit_of(p, u);
         const int arow = w.m_blk * 2 * kBM + static_cast<int>(rank) * kBM;
         const int bcol = w.n_blk * Cfg::kBN + static_cast<int>(rank) * Cfg::kHalfN;
+        int a_class = 0, a_crow = 0, k_shift = 0;  // A_CLS: the tile's class, its row in it
+        if constexpr (A_CLS) {
+          a_class = w.m_blk / p.cls_tiles;
+          a_crow = (w.m_blk - a_class * p.cls_tiles) * 2 * kBM + static_cast<int>(rank) * kBM;
+          k_shift = p.cls_shift[a_class];
+        }
         for (int kb = w.kb_begin; kb < w.kb_end; kb += KB) {
           if (!wait_phase(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, p, kRoleProducer))
             goto pair_producer_done;
@@ -1089,7 +1124,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t b_dst = smem_u32(sB + stage * Cfg::kBStage);
             // both k-blocks always load (a second one past the unit's range is never used by
             // the MMA; past K it is zero fill), so the stage's byte count is fixed
-            if constexpr (!A_MN) {
+            if constexpr (A_CLS) {
+#pragma unroll
+              for (int h = 0; h < KB; ++h) {
+                if (kb + h == 0)  // the first window, zeros before k = 0
+                  tma_load_2d_pair(a_dst + h * Cfg::kAAtom, &cls->first, fb, 0, arow);
+                else
+                  tma_load_2d_pair(a_dst + h * Cfg::kAAtom, &cls->cls[a_class], fb,
+                                   (kb + h) * kBK, a_crow);
+              }
+            } else if constexpr (!A_MN) {
 #pragma unroll
               for (int h = 0; h < KB; ++h)
                 tma_load_2d_pair(a_dst + h * Cfg::kAAtom, &tmA, fb, (kb + h) * kBK, arow);
@@ -1101,7 +1145,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if constexpr (!B_K) {
 #pragma unroll
               for (int j = 0; j < Cfg::kHalfN / 64; ++j)
-                tma_load_2d_pair(b_dst + j * Cfg::kMNBox, &tmB, fb, bcol + j * 64, kb * kBK);
+                tma_load_2d_pair(b_dst + j * Cfg::kMNBox, &tmB, fb, bcol + j * 64,
+                                 kb * kBK - k_shift);
             } else {
 #pragma unroll
               for (int h = 0; h < KB; ++h)
@@ -1211,6 +1256,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
   }
+}
+
+template <bool OUT_F32, bool A_MN, bool B_K>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tg_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmOut,
+                        const __grid_constant__ GemmParams p) {
+  pair_gemm_body<OUT_F32, A_MN, B_K, false>(tmA, tmB, tmOut, p, nullptr);
+}
+
+// The CTA-pair kernel with A read through row classes (float32 partials, forward layout).
+// CLASSES is always kARowClasses (a template so that every unit including this header shares
+// one definition).
+template <int CLASSES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tg_gemm_pair_cls_kernel(const __grid_constant__ AClassMaps tmAc,
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmOut,
+                            const __grid_constant__ GemmParams p) {
+  static_assert(CLASSES == kARowClasses, "one class count");
+  pair_gemm_body<true, false, false, true>(tmAc.first, tmB, tmOut, p, &tmAc);
 }
 
 }  // namespace tg

@@ -26,6 +26,16 @@ cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32) {
   return out_f32 ? launch_layout<true>(l) : launch_layout<false>(l);
 }
 
+cudaError_t launch_gemm_pair_cls(const AClassMaps& cls, const GemmLaunch& l) {
+  if (l.grid <= 0 || (l.grid & 1)) return cudaErrorInvalidConfiguration;
+  auto kern = tg_gemm_pair_cls_kernel<kARowClasses>;
+  constexpr int smem = PairCfgFwd::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<l.grid, kThreads, smem, l.stream>>>(cls, l.b, l.out, l.p);
+  return cudaGetLastError();
+}
+
 cudaError_t gemm_pair_max_clusters(int* out) {
   auto kern = tg_gemm_pair_kernel<false, false, false>;
   constexpr int smem = PairCfgFwd::kSmemBytes;

@@ -29,6 +29,9 @@ cudaError_t launch_gemm_bn128(const GemmLaunch& l, bool out_f32);
 
 // CTA-pair kernel (256 x 256 tiles; l.grid must be even, l.p counts pair tiles).
 cudaError_t launch_gemm_pair(const GemmLaunch& l, bool out_f32);
+// The CTA-pair kernel with A read in place through row classes (float32 output only; l.a is
+// unused, l.p.cls_* describe the classes).
+cudaError_t launch_gemm_pair_cls(const AClassMaps& cls, const GemmLaunch& l);
 // Clusters of two that can be resident at once on the current device.
 cudaError_t gemm_pair_max_clusters(int* out);
 

@@ -104,6 +104,12 @@ typedef struct {
                            -1: never */
   int swap_ab;          /* int4 GEMM only: 0 choose (swapped for M <= 128), 1 compute C^T =
                            W^T A^T with the decoded weights as the 128-row MMA side, -1 never */
+  int a_in_place;       /* 1: an A whose leading dimension is not a multiple of 8 is read in
+                           place through 16 row classes (tg_plan.a_row_classes) instead of being
+                           copied into aligned scratch, when A is 32-byte aligned and the plan
+                           uses CTA pairs.  Saves the copy's M * K * 2 bytes of scratch; on GB300
+                           the copy is faster (4095 x 3073 x 65537: 1.35 against 1.47 ms),
+                           because a class's rows start mid-line in L2.  0: copy */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
@@ -131,6 +137,9 @@ typedef struct {
   int cta_pair;                /* 1: 256x256 tiles on clusters of two CTAs (tcgen05 cta_group::2) */
   int64_t tail_tiles;          /* tiles of the last partial wave computed as two K halves (the
                                   units count both halves); 0 when not used */
+  int a_row_classes;           /* 16: A (leading dimension not a multiple of 8) read in place in
+                                  16 row classes, each tile's rows from one class, instead of
+                                  being repacked (tg_options.a_in_place); 0 otherwise */
 } tg_plan;
 
 /*

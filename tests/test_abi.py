@@ -42,7 +42,7 @@ def test_status_strings(lib):
     for s in range(7):
         assert binding.tg_status_string(s)
     assert binding.tg_status_string(99) == "unknown status"
-    assert binding.tg_version() == 100
+    assert binding.tg_version() == 200
 
 
 def test_validation_before_any_device_work(lib):
@@ -100,15 +100,33 @@ def test_plan_skinny_fills_the_machine(lib):
 
 
 def test_plan_ragged_unaligned(lib):
-    # odd leading dimensions: operands are repacked, C goes through the fp32 workspace
+    # odd leading dimensions: A and B are repacked into 128-byte rows, C goes through the fp32
+    # workspace
     p = _plan(4095, 3073, 65537)
     assert p["repack_a"] == 1 and p["repack_b"] == 1 and p["workspace_epilogue"] == 1
-    assert p["kernels"] == 4
+    assert p["a_row_classes"] == 0 and p["kernels"] == 4
     assert p["kblocks"] == 1025
     assert p["split_k"] * p["kblocks_per_split"] >= 1025
     assert (p["split_k"] - 1) * p["kblocks_per_split"] < 1025
-    ws = 4095 * 65544 * 2 + 65537 * 3080 * 2 + p["split_k"] * 4095 * 3076 * 4
+    ws = 4095 * 65600 * 2 + 65537 * 3136 * 2 + p["split_k"] * 4095 * 3104 * 4
     assert p["workspace_bytes"] >= ws
+    # on request, A (32-byte aligned) is read in place through 16 row classes instead
+    c = _plan(4095, 3073, 65537, options={"a_in_place": 1})
+    assert c["a_row_classes"] == 16 and c["repack_a"] == 0
+    assert c["repack_b"] == 1 and c["workspace_epilogue"] == 1 and c["cta_pair"] == 1
+    assert c["kernels"] == 4  # first-window copy, B repack, GEMM, reduction
+    assert c["tiles_m"] == 16  # 16 classes of 256 rows: no more tiles than 4095 rows need
+    assert c["kblocks"] == 1025  # windows start up to 15 elements early: ceil((K + 15) / 64)
+    wsc = 16 * 256 * 64 * 2 + 65537 * 3136 * 2 + c["split_k"] * 16 * 256 * 3104 * 4
+    assert c["workspace_bytes"] >= wsc and c["workspace_bytes"] < ws
+    # not possible: A only 16-byte aligned (a class base would start before A), a forced
+    # repack, or an M whose class-major order adds tiles (2000 rows: 16 classes of 125 rows,
+    # each in a tile of 256)
+    for kw in ({"a_ptr": 256 + 16}, {"options": {"a_in_place": 1, "force_repack": 1}}):
+        q = _plan(4095, 3073, 65537, **({"options": {"a_in_place": 1}} | kw))
+        assert q["a_row_classes"] == 0 and q["repack_a"] == 1
+    g = _plan(2000, 3073, 65537, options={"a_in_place": 1})
+    assert g["a_row_classes"] == 0 and g["repack_a"] == 1
 
 
 def test_plan_alignment_from_pointers(lib):

@@ -255,3 +255,28 @@ def test_torch_wrapper_and_views():
     assert_parity(C.cpu().numpy().view(np.uint16), oracle_ref(a, b, True), K, True)
     with pytest.raises(TypeError):
         gemm_relu(A.float(), B)
+
+
+@pytest.mark.parametrize("M,N,K,lda,opts", [
+    (4095, 200, 1000, 1001, {"pair": 1, "a_in_place": 1}),
+    (4096, 300, 777, 779, {"pair": 1, "split_k": 3, "a_in_place": 1}),
+    (4095, 136, 64, 65, {"pair": 1, "a_in_place": 1}),  # K in one k-block, padding after rows
+    (8190, 100, 300, 313, {"pair": 1, "split_k": 1, "a_in_place": 1}),
+    (4000, 257, 2000, 2003, {"pair": 1, "max_ctas": 6, "a_in_place": 1}),  # several tiles/cluster
+])
+def test_a_read_by_row_classes(M, N, K, lda, opts):
+    # On request, A with a leading dimension that is not a multiple of 8 is read in place
+    # through 16 row classes (no repack): each class's K windows start up to 15 elements early, the first
+    # window comes from a zero-padded copy, and the partial sums pass through the workspace
+    # in class-major row order.  A's padding holds NaN, so a read outside A's rows would show.
+    st, plan = binding.tg_plan_query(0x100000, 0x200000, 0x300000, M, N, K, lda, N, N, 152, opts)
+    assert st == binding.TG_OK and plan["a_row_classes"] == 16 and plan["repack_a"] == 0
+    a = inputs.tensor(M, K, 71, 0)
+    b = inputs.tensor(K, N, 71, 1)
+    c, pad_ok = run_gpu(a, b, True, opts, lda=lda)
+    assert pad_ok
+    assert_parity(c, oracle_ref(a, b, True), K, True, where=f"row classes {M}x{N}x{K} lda={lda}")
+    ai = inputs.tensor(M, K, 72, 0, "int")
+    bi = inputs.tensor(K, N, 72, 1, "int")
+    ci, _ = run_gpu(ai, bi, True, opts, lda=lda, ldb=N + 3, ldc=N + 1)
+    np.testing.assert_array_equal(ci, oracle.gemm_relu(ai, bi, relu=True, want=("f32",))["out16_f32acc"])
