@@ -30,7 +30,8 @@ TG_DEBUG_DROP_FIRST_STAGE = 1
 class tg_options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "block_n", "split_k", "force_repack", "force_workspace", "panel_m", "max_ctas",
-        "debug_flags", "timeout_ms", "pair", "tail", "swap_ab", "a_in_place")]
+        "debug_flags", "timeout_ms", "pair", "tail", "swap_ab", "a_in_place",
+        "repack_overlap")]
 
 
 class tg_epilogue(ctypes.Structure):
@@ -52,6 +53,7 @@ class tg_plan(ctypes.Structure):
         ("workspace_epilogue", ctypes.c_int), ("workspace_bytes", ctypes.c_int64),
         ("kernels", ctypes.c_int), ("cta_pair", ctypes.c_int),
         ("tail_tiles", ctypes.c_int64), ("a_row_classes", ctypes.c_int),
+        ("repack_overlap", ctypes.c_int),
     ]
 
     def as_dict(self) -> dict:

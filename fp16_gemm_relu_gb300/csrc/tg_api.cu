@@ -21,6 +21,7 @@ constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;  // TMA coordinates are 3
 constexpr int kDefaultPanel = 16;
 constexpr int kDefaultTimeoutMs = 2000;
 constexpr int kBlockNs[3] = {256, 192, 128};
+constexpr int kMaxOverlapSplits = 32;  // the plan's largest split count
 
 thread_local int t_last_cuda_error = 0;
 
@@ -41,9 +42,46 @@ struct DeviceState {
   int pair_clusters = 0;  // co-resident clusters of the CTA-pair kernel (0: do not use it)
 };
 
+// Library streams and events of the overlapped operand copies (one set per device, created on
+// first use): `copy` makes the split-by-split copies, gemm[0] / gemm[1] take the splits' GEMMs
+// in turn so that one split's last partial wave can share the SMs with the next split's
+// first.  Calls enqueue under `mu`; each joins every stream back to the caller's before it
+// returns, so work of different calls only meets in stream order.
+struct OverlapStreams {
+  bool ready = false;
+  cudaStream_t copy = nullptr, gemm[2] = {nullptr, nullptr};
+  cudaEvent_t start = nullptr, copied[kMaxOverlapSplits] = {}, done[3] = {};
+  std::mutex mu;
+};
+
 constexpr int kMaxDevices = 64;
 DeviceState g_devices[kMaxDevices];
+OverlapStreams g_overlap[kMaxDevices];
 std::mutex g_mutex;
+
+tg_status overlap_streams(OverlapStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return TG_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  OverlapStreams& o = g_overlap[dev];
+  if (!o.ready) {
+    const unsigned ev = cudaEventDisableTiming;
+    if ((e = cudaStreamCreateWithFlags(&o.copy, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&o.gemm[0], cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&o.gemm[1], cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&o.start, ev)) != cudaSuccess)
+      return cuda_fail(e);
+    for (int i = 0; i < kMaxOverlapSplits; ++i)
+      if ((e = cudaEventCreateWithFlags(&o.copied[i], ev)) != cudaSuccess) return cuda_fail(e);
+    for (int i = 0; i < 3; ++i)
+      if ((e = cudaEventCreateWithFlags(&o.done[i], ev)) != cudaSuccess) return cuda_fail(e);
+    o.ready = true;
+  }
+  *out = &o;
+  return TG_OK;
+}
 
 tg_status current_device(DeviceState** out) {
   int dev = 0;
@@ -166,7 +204,8 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 192 && o.block_n != 256)
     return TG_ERR_INVALID_ARG;
   if (o.split_k < 0 || o.panel_m < 0 || o.max_ctas < 0 || o.timeout_ms < 0 || o.pair < -1 ||
-      o.pair > 1 || o.tail < -1 || o.tail > 1 || o.a_in_place < 0 || o.a_in_place > 1)
+      o.pair > 1 || o.tail < -1 || o.tail > 1 || o.a_in_place < 0 || o.a_in_place > 1 ||
+      o.repack_overlap < -1 || o.repack_overlap > 0)
     return TG_ERR_INVALID_ARG;
   if (o.pair == 1 && o.block_n != 0 && o.block_n != 256) return TG_ERR_INVALID_ARG;
 
@@ -347,7 +386,16 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
     off += pl.tail_cnt_bytes;
   }
   P.workspace_bytes = off;
-  P.kernels = 1 + P.repack_a + P.repack_b + P.workspace_epilogue + (P.a_row_classes ? 1 : 0);
+  // Operand copies overlap the GEMM split by split: split s's slice of A and B is copied on a
+  // library stream while the GEMMs of earlier splits run (the copies use DRAM bandwidth that
+  // the L2-bound GEMM leaves idle), and each split's GEMM starts once its slice is in place.
+  P.repack_overlap = (P.repack_a || P.repack_b) && P.split_k >= 2 && P.workspace_epilogue &&
+                     !P.tail_tiles && !P.a_row_classes && o.repack_overlap >= 0 &&
+                     P.split_k <= kMaxOverlapSplits;
+  if (P.repack_overlap)
+    P.kernels = P.split_k * (1 + P.repack_a + P.repack_b) + 1;
+  else
+    P.kernels = 1 + P.repack_a + P.repack_b + P.workspace_epilogue + (P.a_row_classes ? 1 : 0);
   *out = pl;
   return TG_OK;
 }
@@ -484,10 +532,16 @@ __global__ void tg_relu_backward_kernel(const uint16_t* __restrict__ dC, int64_t
   }
 }
 
-int aux_grid(int64_t work_items, int num_sms) {
+int aux_grid(int64_t work_items, int num_sms, int per_sm = 8) {
   const int64_t blocks = cdiv(std::max<int64_t>(work_items, 1), 256);
-  return static_cast<int>(std::min<int64_t>(blocks, int64_t(num_sms) * 8));
+  return static_cast<int>(std::min<int64_t>(blocks, int64_t(num_sms) * per_sm));
 }
+
+// Blocks per SM of the operand copies that run beside the GEMM (overlapped copies).  On
+// 4095 x 3073 x 65537 (two runs each): 1 block 1.62 ms per step, 2: 1.43, 4: 1.32, 8: 1.33;
+// copies first, no overlap: 1.33-1.38.  With fewer blocks the copies themselves become the
+// critical path.
+constexpr int kOverlapCopyBlocksPerSm = 4;
 
 CUresult encode_2d(PFN_cuTensorMapEncodeTiled_v12000 enc, CUtensorMap* m,
                    CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
@@ -585,21 +639,52 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   const void* Ae = A;
   const void* Be = B;
   int64_t lda_e = lda, ldb_e = ldb;
+  uint16_t* Ap = P.repack_a ? reinterpret_cast<uint16_t*>(scratch + pl.off_a) : nullptr;
+  uint16_t* Bp = P.repack_b ? reinterpret_cast<uint16_t*>(scratch + pl.off_b) : nullptr;
+  // Copies of the K range [k0, k1) of A and B into their aligned scratch (A stored M x K:
+  // columns k0..k1 of every row; stored K x M: rows k0..k1; B likewise).
+  auto copy_k_range = [&](int64_t k0, int64_t k1, cudaStream_t st, int per_sm) -> cudaError_t {
+    const uint16_t* a16 = static_cast<const uint16_t*>(A);
+    const uint16_t* b16 = static_cast<const uint16_t*>(B);
+    if (P.repack_a) {
+      if (ta)
+        tg_pack_rows_kernel<<<aux_grid((k1 - k0) * cdiv(M, 8), ds->sm_count, per_sm), 256, 0, st>>>(
+            a16 + k0 * lda, lda, Ap + k0 * pl.lda_p, pl.lda_p, k1 - k0, M);
+      else
+        tg_pack_rows_kernel<<<aux_grid(M * cdiv(k1 - k0, 8), ds->sm_count, per_sm), 256, 0, st>>>(
+            a16 + k0, lda, Ap + k0, pl.lda_p, M, k1 - k0);
+      const cudaError_t ce = cudaGetLastError();
+      if (ce != cudaSuccess) return ce;
+    }
+    if (P.repack_b) {
+      if (tb)
+        tg_pack_rows_kernel<<<aux_grid(N * cdiv(k1 - k0, 8), ds->sm_count, per_sm), 256, 0, st>>>(
+            b16 + k0, ldb, Bp + k0, pl.ldb_p, N, k1 - k0);
+      else
+        tg_pack_rows_kernel<<<aux_grid((k1 - k0) * cdiv(N, 8), ds->sm_count, per_sm), 256, 0, st>>>(
+            b16 + k0 * ldb, ldb, Bp + k0 * pl.ldb_p, pl.ldb_p, k1 - k0, N);
+      return cudaGetLastError();
+    }
+    return cudaSuccess;
+  };
   if (P.repack_a) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pl.off_a);
-    tg_pack_rows_kernel<<<aux_grid(M * cdiv(K, 8), ds->sm_count), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(A), lda, dst, pl.lda_p, ta ? K : M, ta ? M : K);
-    if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
-    Ae = dst;
+    Ae = Ap;
     lda_e = pl.lda_p;
   }
   if (P.repack_b) {
-    uint16_t* dst = reinterpret_cast<uint16_t*>(scratch + pl.off_b);
-    tg_pack_rows_kernel<<<aux_grid(K * cdiv(N, 8), ds->sm_count), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(B), ldb, dst, pl.ldb_p, tb ? N : K, tb ? K : N);
-    if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
-    Be = dst;
+    Be = Bp;
     ldb_e = pl.ldb_p;
+  }
+  // Under stream capture the library's side streams would join the caller's graph (and could
+  // meet another thread's eager calls there): a captured call takes the sequential path.
+  bool overlap = P.repack_overlap != 0;
+  if (overlap) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) return fail(cuda_fail(e));
+    overlap = cap == cudaStreamCaptureStatusNone;
+  }
+  if (!overlap && (P.repack_a || P.repack_b)) {
+    if ((e = copy_k_range(0, K, stream, 8)) != cudaSuccess) return fail(cuda_fail(e));
   }
 
   tg::GemmLaunch L;
@@ -697,16 +782,58 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   }
   L.grid = P.grid;
   L.stream = stream;
-  if (P.a_row_classes) {
-    e = tg::launch_gemm_pair_cls(cls, L);
-  } else if (P.cta_pair) {
-    e = tg::launch_gemm_pair(L, ws != nullptr);
-  } else switch (P.block_n) {
-    case 256: e = tg::launch_gemm_bn256(L, ws != nullptr); break;
-    case 192: e = tg::launch_gemm_bn192(L, ws != nullptr); break;
-    default: e = tg::launch_gemm_bn128(L, ws != nullptr); break;
+  auto launch = [&](const tg::GemmLaunch& l) -> cudaError_t {
+    if (P.a_row_classes) return tg::launch_gemm_pair_cls(cls, l);
+    if (P.cta_pair) return tg::launch_gemm_pair(l, ws != nullptr);
+    switch (P.block_n) {
+      case 256: return tg::launch_gemm_bn256(l, ws != nullptr);
+      case 192: return tg::launch_gemm_bn192(l, ws != nullptr);
+      default: return tg::launch_gemm_bn128(l, ws != nullptr);
+    }
+  };
+  if (!overlap) {
+    if ((e = launch(L)) != cudaSuccess) return fail(cuda_fail(e));
+  } else {
+    // split s: copy its K slice on ov->copy, then its GEMM (the tiles of split s only) on
+    // ov->gemm[s & 1] once the slice is in place; every stream joins back to `stream` before
+    // the reduction, on success and on error alike (the scratch is freed on `stream`).
+    OverlapStreams* ov = nullptr;
+    if ((st = overlap_streams(&ov)) != TG_OK) return fail(st);
+    std::lock_guard<std::mutex> lock(ov->mu);
+    cudaError_t ce = cudaEventRecord(ov->start, stream);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(ov->copy, ov->start, 0);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(ov->gemm[0], ov->start, 0);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(ov->gemm[1], ov->start, 0);
+    const int64_t tiles = P.tiles_m * P.tiles_n;
+    const int64_t kspan = P.kblocks_per_split * tg::kBK;
+    for (int sp = 0; sp < P.split_k && ce == cudaSuccess; ++sp) {
+      const int64_t k0 = sp * kspan, k1 = std::min<int64_t>(K, k0 + kspan);
+      cudaStream_t g = ov->gemm[sp & 1];
+      // the first split's copy has the GPU to itself
+      ce = copy_k_range(k0, k1, ov->copy, sp == 0 ? 8 : kOverlapCopyBlocksPerSm);
+      if (ce == cudaSuccess) ce = cudaEventRecord(ov->copied[sp], ov->copy);
+      if (ce == cudaSuccess) ce = cudaStreamWaitEvent(g, ov->copied[sp], 0);
+      if (ce != cudaSuccess) break;
+      tg::GemmLaunch ls = L;
+      ls.p.unit_base = static_cast<int>(sp * tiles);
+      ls.p.units = static_cast<int>(tiles);
+      ls.grid = P.cta_pair ? 2 * static_cast<int>(std::min<int64_t>(tiles, P.grid / 2))
+                           : static_cast<int>(std::min<int64_t>(tiles, P.grid));
+      ls.stream = g;
+      ce = launch(ls);
+    }
+    cudaError_t je = cudaEventRecord(ov->done[0], ov->copy);
+    if (je == cudaSuccess) je = cudaEventRecord(ov->done[1], ov->gemm[0]);
+    if (je == cudaSuccess) je = cudaEventRecord(ov->done[2], ov->gemm[1]);
+    for (int i = 0; i < 3 && je == cudaSuccess; ++i) je = cudaStreamWaitEvent(stream, ov->done[i], 0);
+    if (je != cudaSuccess) {  // cannot order the side streams: wait for them here
+      cudaStreamSynchronize(ov->copy);
+      cudaStreamSynchronize(ov->gemm[0]);
+      cudaStreamSynchronize(ov->gemm[1]);
+    }
+    if (ce == cudaSuccess) ce = je;
+    if (ce != cudaSuccess) return fail(cuda_fail(ce));
   }
-  if (e != cudaSuccess) return fail(cuda_fail(e));
 
   if (ws) {
     tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(

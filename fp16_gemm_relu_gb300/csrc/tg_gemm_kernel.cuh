@@ -52,7 +52,9 @@ struct GemmParams {
   int num_kb;          // ceil(K / kBK)
   int kb_per_split;
   int splits;
-  int units;           // tiles_m * tiles_n * splits
+  int units;           // work units of this launch: tiles_m * tiles_n * splits, or the
+                       // tiles of one split when a plan launches its splits one by one
+  int unit_base;       // unit number of this launch's first unit (0, or split * tiles)
   int panel_m;
   int act;             // epilogue activation: kActNone, kActRelu, kActGelu, kActGeluTanh
   int a_mn;            // 1: A is stored K x M (M contiguous): MN-major tiles, two 64-wide boxes
@@ -436,6 +438,7 @@ struct Unit {
 // With p.tail, units past n_full are K halves of the last tiles (tile n_full + slot).
 __device__ __forceinline__ Unit unit_of(const GemmParams& p, int u) {
   Unit w;
+  u += p.unit_base;
   const int tiles = p.tiles_m * p.tiles_n;
   int t;
   w.tail_slot = -1;

@@ -110,6 +110,8 @@ typedef struct {
                            uses CTA pairs.  Saves the copy's M * K * 2 bytes of scratch; on GB300
                            the copy is faster (4095 x 3073 x 65537: 1.35 against 1.47 ms),
                            because a class's rows start mid-line in L2.  0: copy */
+  int repack_overlap;   /* 0: choose (tg_plan.repack_overlap); -1: never overlap the operand
+                           copies with the GEMM */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
@@ -140,6 +142,13 @@ typedef struct {
   int a_row_classes;           /* 16: A (leading dimension not a multiple of 8) read in place in
                                   16 row classes, each tile's rows from one class, instead of
                                   being repacked (tg_options.a_in_place); 0 otherwise */
+  int repack_overlap;          /* 1: with split-K and operand copies, the copies are made split
+                                  by split on a library stream, each split's GEMM launched (on
+                                  two more library streams, in turn) as soon as its slice is
+                                  copied, so copies overlap the GEMMs of earlier splits; all
+                                  streams join the caller's stream before the reduction.  A
+                                  call made under stream capture runs the copies first instead.
+                                  0: copies first, then one GEMM launch */
 } tg_plan;
 
 /*

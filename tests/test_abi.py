@@ -104,8 +104,12 @@ def test_plan_ragged_unaligned(lib):
     # workspace
     p = _plan(4095, 3073, 65537)
     assert p["repack_a"] == 1 and p["repack_b"] == 1 and p["workspace_epilogue"] == 1
-    assert p["a_row_classes"] == 0 and p["kernels"] == 4
-    assert p["kblocks"] == 1025
+    assert p["a_row_classes"] == 0 and p["kblocks"] == 1025
+    # the copies overlap the GEMMs split by split: per split two copies and one GEMM, then
+    # one reduction
+    assert p["repack_overlap"] == 1 and p["kernels"] == 3 * p["split_k"] + 1
+    q = _plan(4095, 3073, 65537, options={"repack_overlap": -1})
+    assert q["repack_overlap"] == 0 and q["kernels"] == 4
     assert p["split_k"] * p["kblocks_per_split"] >= 1025
     assert (p["split_k"] - 1) * p["kblocks_per_split"] < 1025
     ws = 4095 * 65600 * 2 + 65537 * 3136 * 2 + p["split_k"] * 4095 * 3104 * 4
@@ -123,8 +127,8 @@ def test_plan_ragged_unaligned(lib):
     # repack, or an M whose class-major order adds tiles (2000 rows: 16 classes of 125 rows,
     # each in a tile of 256)
     for kw in ({"a_ptr": 256 + 16}, {"options": {"a_in_place": 1, "force_repack": 1}}):
-        q = _plan(4095, 3073, 65537, **({"options": {"a_in_place": 1}} | kw))
-        assert q["a_row_classes"] == 0 and q["repack_a"] == 1
+        r = _plan(4095, 3073, 65537, **({"options": {"a_in_place": 1}} | kw))
+        assert r["a_row_classes"] == 0 and r["repack_a"] == 1
     g = _plan(2000, 3073, 65537, options={"a_in_place": 1})
     assert g["a_row_classes"] == 0 and g["repack_a"] == 1
 
