@@ -72,10 +72,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+# Sources of the kernels a bench line times: the fp16 GEMMs (and the host code that plans and
+# launches them), plus the dequantising kernels for the int4 / NF4 lines.
+DENSE_SOURCES = ["tg_api.cu", "tg_gemm_kernel.cuh", "tg_gemm_pair.cu", "tg_gemm_bn128.cu",
+                 "tg_gemm_bn192.cu", "tg_gemm_bn256.cu", "tg_internal.h"]
+DEQUANT_SOURCES = DENSE_SOURCES + ["tg_gemm_w4.cuh", "tg_gemm_w4.cu"]
+
+
+def kernel_source_hash(dequant: bool = False) -> str:
+    """Hash of the sources behind a measured kernel (the dense set, or with the dequantising
+    kernels); a committed ncu summary applies while its hash matches."""
     csrc = os.path.join(ROOT, "fp16_gemm_relu_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(DEQUANT_SOURCES if dequant else DENSE_SOURCES):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -99,7 +108,7 @@ def traffic_from_profiles(workload: str):
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(dequant=any(t in workload.split("/") for t in ("w4", "nf4")))
     for line in open(path):
         parts = line.split()
         if len(parts) >= 3 and parts[0] == workload and parts[1] == cur:
