@@ -10,11 +10,11 @@ namespace {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int BMT, int FMT>
+template <int BMT, int FMT, bool TDEC = false>
 cudaError_t launch_w4t(const CUtensorMap& a, const CUtensorMap& q, const CUtensorMap& s,
                        const tg::GemmParams& p, int grid, cudaStream_t stream) {
-  auto kern = tg::tg_gemm_w4t_kernel<BMT, FMT>;
-  constexpr int smem = tg::W4TCfg<BMT>::kSmemBytes;
+  auto kern = tg::tg_gemm_w4t_kernel<BMT, FMT, TDEC>;
+  constexpr int smem = tg::W4TCfg<BMT, TDEC>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, tg::kW4TThreads, smem, stream>>>(a, q, s, p);
@@ -131,7 +131,8 @@ tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C
   if (opt) o = *opt;
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256) return TG_ERR_INVALID_ARG;
   if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0 || o.swap_ab < -1 || o.swap_ab > 1 ||
-      o.pair < -1 || o.pair > 1 || o.tail < -1 || o.tail > 1)
+      o.pair < -1 || o.pair > 1 || o.tail < -1 || o.tail > 1 || o.tmem_decode < 0 ||
+      o.tmem_decode > 1)
     return TG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TG_OK;
   if (C == nullptr) return TG_ERR_INVALID_ARG;
@@ -214,8 +215,12 @@ tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C
       }
     }
     const int grid = static_cast<int>(std::min<int64_t>(p.units, grid_cap0));
-    const cudaError_t ce = bmt == 64 ? launch_w4t<64, FMT>(ta, tq, ts, p, grid, stream)
-                                     : launch_w4t<128, FMT>(ta, tq, ts, p, grid, stream);
+    // on request, with 64 rows of A (the accumulators then leave half of tensor memory for
+    // decoded stages), the weights are decoded into tensor memory
+    const bool tdec = bmt == 64 && o.tmem_decode > 0;
+    const cudaError_t ce = bmt == 128 ? launch_w4t<128, FMT>(ta, tq, ts, p, grid, stream)
+                           : tdec     ? launch_w4t<64, FMT, true>(ta, tq, ts, p, grid, stream)
+                                      : launch_w4t<64, FMT>(ta, tq, ts, p, grid, stream);
     const cudaError_t fe = scratch ? cudaFreeAsync(scratch, stream) : cudaSuccess;
     if (ce != cudaSuccess) return tg::record_cuda_error(ce);
     return fe == cudaSuccess ? TG_OK : tg::record_cuda_error(fe);

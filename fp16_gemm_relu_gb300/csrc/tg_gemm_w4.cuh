@@ -54,6 +54,41 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return __byte_perm(a, b, sel);
 }
 
+// ---- tensor-memory operand path of the swapped kernel (TDEC) ----
+// D[tmem] (+)= A[tmem] * B[smem desc]: A (M = 128 rows in TMEM lanes, 16 k as eight 32-bit
+// columns of fp16 pairs, k even in the low half) read from tensor memory.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns from registers: thread l writes lane
+// (base + l).  Like tcgen05.ld, a .sync.aligned instruction: the warp is reconverged first.
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  __syncwarp();
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Wait until this thread's tcgen05.st have written tensor memory.
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+
 enum : int { kFmtInt4 = 0, kFmtNf4 = 1 };
 
 // PTX prmt.b32 in its default mode: result byte i is byte (c >> 4i) & 7 of {b, a} (a holds
@@ -154,6 +189,30 @@ __device__ __forceinline__ void scale_pairs(const uint4& sv, uint32_t (&sp)[4]) 
     sp[2] = sv.z;
     sp[3] = sv.w;
   }
+}
+
+// Two weights of one column in consecutive K rows, t0 and t1 holding each row's nibble in
+// bits 0-3 (higher bits are ignored), scaled by s2 = (s, s): fp16 pair (row k low, k + 1 high).
+template <int FMT>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t t0, uint32_t t1, uint32_t s2) {
+  uint32_t c;
+  if constexpr (FMT == kFmtInt4) {
+    // (1024 + q0, 1024 + q1) as fp16, minus 1032: q - 8 exactly
+    const uint32_t x = (prmt_ptx(t0, t1, 0x5410u) & 0x000F000Fu) | 0x64006400u;
+    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), k1032);
+    c = *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const uint32_t v = prmt_ptx(t0, t1, 0x0040u);          // byte 0: t0's, byte 1: t1's low byte
+    const uint32_t sel = (v & 0x7u) | ((v >> 4) & 0x70u);  // nibbles q0 & 7, q1 & 7
+    const uint32_t hi8 = prmt_ptx(v << 4, 0u, 0x0098u);    // byte i: 0xFF where q_i >= 8
+    const uint32_t lo = lut16x4(kNf4Lo0, kNf4Lo1, kNf4Lo2, kNf4Lo3, sel, hi8);
+    const uint32_t hi = lut16x4(kNf4Hi0, kNf4Hi1, kNf4Hi2, kNf4Hi3, sel, hi8);
+    c = prmt_ptx(lo, hi, 0x5140u);                         // (code q0, code q1)
+  }
+  const __half2 w = __hmul2(*reinterpret_cast<const __half2*>(&c),
+                            *reinterpret_cast<const __half2*>(&s2));  // one rounding
+  return *reinterpret_cast<const uint32_t*>(&w);
 }
 
 template <int FMT>
@@ -731,11 +790,16 @@ constexpr int kW4TDeqWarps = kW4TDeqGroups * kW4TGroupWarps;
 constexpr int kW4TMma2Warp = 2 + kEpiWarps + kW4TDeqWarps;  // second MMA issuer
 constexpr int kW4TThreads = (3 + kEpiWarps + kW4TDeqWarps) * 32;
 
-template <int BMT>
+// TDEC: the dequantisers write the decoded tile into tensor memory instead of shared memory,
+// and the MMA reads its A operand (the decoded weights) from there.  Each dequantiser thread
+// owns one TMEM lane = one output column of the tile and writes that column's 64 weights of a
+// stage as 32 columns of fp16 pairs (k even in the low half).  A stage's slot sits after the
+// accumulators; the slots form the same ring as the shared-memory stages.
+template <int BMT, bool TDEC = false>
 struct W4TCfg {
   static constexpr int kNTile = 128;                  // output columns per tile (MMA M)
   static constexpr int kActStage = BMT * kBK * 2;     // activations, K-major
-  static constexpr int kDecStage = kBK * kNTile * 2;  // decoded weights, MN-major
+  static constexpr int kDecStage = TDEC ? 0 : kBK * kNTile * 2;  // decoded weights, MN-major
   static constexpr int kQStage = kBK * kNTile / 2;
   static constexpr int kSStage = 1024;
   static constexpr int kStageBytes = kActStage + kDecStage + kQStage + kSStage;
@@ -744,9 +808,12 @@ struct W4TCfg {
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kAccStride = BMT;              // TMEM columns per accumulator
   // two TMEM buffers x two accumulators (even and odd k-blocks of a unit)
-  static constexpr int kTmemCols = 4 * BMT < 32 ? 32 : 4 * BMT;
+  static constexpr int kAccCols = 4 * BMT < 32 ? 32 : 4 * BMT;
+  static constexpr int kDecCols = kBK / 2;            // TMEM columns of one decoded stage
+  static constexpr int kTmemCols = TDEC ? 512 : kAccCols;
   static constexpr int kSmemBytes = kSmemReserve + kStages * kStageBytes;
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget exceeded");
+  static_assert(!TDEC || kAccCols + kStages * kDecCols <= 512, "TMEM ring exceeds 512 columns");
 };
 
 // tmA: fp16 A {K, M} box {64, BMT} SW128 (K-major operand of the transposed product);
@@ -754,12 +821,12 @@ struct W4TCfg {
 // p.tiles_n counts 128-column blocks of C.  p.splits == 1.  With p.tail, units [0, n_full)
 // are whole tiles and each later tile is two units, one per K half (see unit_of); tail_ws
 // holds 2 x 4 x 32 x BMT floats per split tile and tail_cnt 4 zeroed counters per split tile.
-template <int BMT, int FMT>
+template <int BMT, int FMT, bool TDEC>
 __global__ void __launch_bounds__(kW4TThreads, 1)
     tg_gemm_w4t_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmS, const GemmParams p) {
-  using Cfg = W4TCfg<BMT>;
+  using Cfg = W4TCfg<BMT, TDEC>;
   constexpr int S = Cfg::kStages;
   constexpr int W = Cfg::kNTile / 8;  // 16 packed words per row
 
@@ -859,8 +926,9 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
     // of each unit into accumulator j of the unit's TMEM buffer; the epilogue adds the two.
     if (lane == 0) {
       const int j = warp == 1 ? 0 : 1;
-      // D (128 n x BMT m) += Wdec (128 n x 16 k, MN-major) * A^T (16 k x BMT m, K-major)
-      const uint32_t idesc = idesc_f16_f32(Cfg::kNTile, BMT, 1, 0);
+      // D (128 n x BMT m) += Wdec (128 n x 16 k, MN-major in shared memory, or K-major in
+      // tensor memory) * A^T (16 k x BMT m, K-major)
+      const uint32_t idesc = idesc_f16_f32(Cfg::kNTile, BMT, TDEC ? 0 : 1, 0);
       int stage = 0;
       uint32_t phase = 0;
       int t = 0;
@@ -887,12 +955,22 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = desc_mnmajor(smem_u32(sDec + stage * Cfg::kDecStage));
           const uint64_t bd = desc_kmajor(smem_u32(sAct + stage * Cfg::kActStage));
+          if constexpr (TDEC) {
+            // the stage's decoded slot: 16 k = 8 columns per MMA
+            const uint32_t a_tmem =
+                tmem_base + static_cast<uint32_t>(Cfg::kAccCols + stage * Cfg::kDecCols);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_f16(d_tmem, ad + 128u * k, bd + 2u * k, idesc,
-                     (kb - w.kb_begin > 1 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              umma_f16_ts(d_tmem, a_tmem + 8u * k, bd + 2u * k, idesc,
+                          (kb - w.kb_begin > 1 || k > 0) ? 1u : 0u);
+          } else {
+            const uint64_t ad = desc_mnmajor(smem_u32(sDec + stage * Cfg::kDecStage));
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              umma_f16(d_tmem, ad + 128u * k, bd + 2u * k, idesc,
+                       (kb - w.kb_begin > 1 || k > 0) ? 1u : 0u);
+          }
           umma_commit(smem_u32(&empty[stage]));
           if (++stage == S) {
             stage = 0;
@@ -937,7 +1015,8 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           tmem_wait_ld(r);
         }
       };
-      const int n = w.n_blk * Cfg::kNTile + decoded_column<FMT>(q * 32 + lane);  // TMEM lane -> column
+      // TMEM lane -> output column (a TMEM-decoded tile keeps the columns in order)
+      const int n = w.n_blk * Cfg::kNTile + (TDEC ? q * 32 + lane : decoded_column<FMT>(q * 32 + lane));
       const int m_base = w.m_blk * BMT;
       const bool n_ok = n < p.N;
       const float bias = (n_ok && p.bias) ? __half2float(p.bias[n]) : 0.0f;
@@ -1040,24 +1119,47 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
           ok = false;
           break;
         }
-        const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
-        uint32_t sp[4];
-        scale_pairs<FMT>(sv, sp);
-        const uint32_t* qw = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
-        uint8_t* ddst = sDec + stage * Cfg::kDecStage + box * 8192;
-        constexpr int kRows = 64 / kRowStep;
-        uint32_t words[kRows];
+        if constexpr (TDEC) {
+          // this thread's TMEM lane is tile column nl: its nibble of word column nl / 8 in each
+          // of the stage's 64 rows, decoded in k pairs and written as 32 TMEM columns
+          const int nl = (warp & 3) * 32 + lane;
+          const uint32_t sh = 4u * static_cast<uint32_t>(nl & 7);
+          const uint32_t sb =
+              reinterpret_cast<const uint16_t*>(sS + stage * Cfg::kSStage)[nl];
+          const uint32_t s2 = sb | (sb << 16);
+          const uint32_t* col =
+              reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage) + (nl >> 3);
+          uint32_t r[32];
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) words[i] = qw[(row_first + i * kRowStep) * W + cw];
+          for (int j = 0; j < 32; ++j)
+            r[j] = decode_pair<FMT>(col[(2 * j) * W] >> sh, col[(2 * j + 1) * W] >> sh, s2);
+          const uint32_t taddr = tmem_base + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                                 static_cast<uint32_t>(Cfg::kAccCols + stage * Cfg::kDecCols);
+          tmem_st_x32(taddr, r);
+          tmem_wait_st();
+          tc_fence_before();  // the MMA thread reads these columns after the barrier
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&deq_full[stage]));
+        } else {
+          const uint4 sv = *reinterpret_cast<const uint4*>(sS + stage * Cfg::kSStage + cw * 16);
+          uint32_t sp[4];
+          scale_pairs<FMT>(sv, sp);
+          const uint32_t* qw = reinterpret_cast<const uint32_t*>(sQ + stage * Cfg::kQStage);
+          uint8_t* ddst = sDec + stage * Cfg::kDecStage + box * 8192;
+          constexpr int kRows = 64 / kRowStep;
+          uint32_t words[kRows];
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) {
-          const int r = row_first + i * kRowStep;
-          const uint4 v = decode8<FMT>(words[i], sp);
-          *reinterpret_cast<uint4*>(ddst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
+          for (int i = 0; i < kRows; ++i) words[i] = qw[(row_first + i * kRowStep) * W + cw];
+#pragma unroll
+          for (int i = 0; i < kRows; ++i) {
+            const int r = row_first + i * kRowStep;
+            const uint4 v = decode8<FMT>(words[i], sp);
+            *reinterpret_cast<uint4*>(ddst + r * 128 + ((chunk ^ (r & 7)) << 4)) = v;
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&deq_full[stage]));
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&deq_full[stage]));
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;

@@ -112,6 +112,11 @@ typedef struct {
                            because a class's rows start mid-line in L2.  0: copy */
   int repack_overlap;   /* 0: choose (tg_plan.repack_overlap); -1: never overlap the operand
                            copies with the GEMM */
+  int tmem_decode;      /* int4 / NF4 GEMM, swapped kernel with M <= 64: 1 decode the weights
+                           into tensor memory, where the MMA reads them (each thread gathers
+                           its column's nibbles row by row: slower than the default on every
+                           shape measured, e.g. 64 x 28672 x 8192 int4 111 against 93 us);
+                           0 decode into shared memory */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
@@ -208,7 +213,8 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
  * once, 256 x 256 tiles on CTA pairs, each CTA decoding half of the weight tile (opt->pair:
  * 1 force, -1 never); else single-CTA 128 x block_n tiles (opt->block_n 128 or 256, which
  * also selects this kernel).  opt may also set max_ctas (a pair counts as two CTAs), tail
- * (swapped kernel: the last partial wave's tiles as two K halves), panel_m and timeout_ms.
+ * (swapped kernel: the last partial wave's tiles as two K halves), tmem_decode, panel_m,
+ * timeout_ms and debug_flags.
  * A split tail takes stream-ordered scratch from the library's pool (TG_ERR_NO_WORKSPACE if
  * unavailable).  Misaligned arguments return TG_ERR_MISALIGNED; asynchronous on `stream`.
  */

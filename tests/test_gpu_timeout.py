@@ -60,7 +60,7 @@ def test_host_entry_reports_clean_status():
 
 
 @pytest.mark.parametrize("fmt", ["int4", "nf4"])
-@pytest.mark.parametrize("kernel", ["swapped", "single_cta", "cta_pair"])
+@pytest.mark.parametrize("kernel", ["swapped", "swapped_tmem", "single_cta", "cta_pair"])
 def test_dequant_kernels_dropped_stage_times_out(fmt, kernel):
     # the same injected fault in the three dequantising GEMM kernels: their waits are bounded
     # like the fp16 kernels'; after the timeout the next call on the context is correct
@@ -71,9 +71,11 @@ def test_dequant_kernels_dropped_stage_times_out(fmt, kernel):
     build.build()
     torch.cuda.set_device(0)
     binding.tg_device_error_check(clear=True)
-    M, N, K, G = 256, 512, 2048, 128
+    # "swapped_tmem": 64 rows of A, weights decoded into tensor memory on request
+    M, N, K, G = (64 if kernel == "swapped_tmem" else 256), 512, 2048, 128
     a, Wq, S = make(M, N, K, G, 41)
-    base = {"swapped": {"swap_ab": 1}, "single_cta": {"swap_ab": -1, "block_n": 128},
+    base = {"swapped": {"swap_ab": 1}, "swapped_tmem": {"swap_ab": 1, "tmem_decode": 1},
+            "single_cta": {"swap_ab": -1, "block_n": 128},
             "cta_pair": {"swap_ab": -1, "pair": 1}}[kernel]
     opts = dict(base, debug_flags=binding.TG_DEBUG_DROP_FIRST_STAGE, timeout_ms=200)
     fn = binding.tg_gemm_w4a16_f16 if fmt == "int4" else binding.tg_gemm_nf4a16_f16

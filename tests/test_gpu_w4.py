@@ -213,3 +213,21 @@ def test_w4_pair_fused_epilogue(act):
     got = run_w4(a, Wq, S, N, G, act=ACT[act], bias=bias, residual=res,
                  options={"pair": 1, "max_ctas": 4})
     check(got, a, Wq, S, N, G, act, bias, res)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nf4"])
+@pytest.mark.parametrize("M,N,K,G", [(1, 257, 640, 128), (37, 1300, 1030, 64), (64, 2048, 4096, 128),
+                                     (64, 520, 64, 64)])
+def test_tmem_decode_matches_shared_memory_decode(fmt, M, N, K, G):
+    # on request, with at most 64 rows of A, the swapped kernel decodes the weights into
+    # tensor memory and the MMA reads them there; the same weights in the same K order through
+    # shared memory must give the same bits, and both match the oracle (default grid with the
+    # split tail, and a small grid with several tiles per CTA)
+    a, Wq, S = make(M, N, K, G, 51)
+    bias = inputs.tensor(1, N, 52, 0).ravel()
+    for extra in ({}, {"max_ctas": 3}):
+        t = run_w4(a, Wq, S, N, G, act=1, bias=bias,
+                   options={"swap_ab": 1, "tmem_decode": 1, **extra}, fmt=fmt)
+        sm = run_w4(a, Wq, S, N, G, act=1, bias=bias, options={"swap_ab": 1, **extra}, fmt=fmt)
+        np.testing.assert_array_equal(t, sm)
+        check(t, a, Wq, S, N, G, "relu", bias, fmt=fmt)

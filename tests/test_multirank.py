@@ -80,13 +80,16 @@ def test_traffic_rows_are_per_variant(tmp_path, monkeypatch):
     assert (bench.traffic_key("square8192", "backward", "gelu", "none")
             == "square8192/backward/gelu")
     (tmp_path / "profiles").mkdir()
-    h = bench.kernel_source_hash()
+    h, hq = bench.kernel_source_hash(), bench.kernel_source_hash(dequant=True)
+    assert h != hq  # the dequantising lines also hash the int4/NF4 kernels
     (tmp_path / "profiles" / "traffic.txt").write_text(
-        f"# header\nsquare8192 {h} 100\nsquare8192/w4 {h} 200\nskinny {h[::-1]} 300\n")
+        f"# header\nsquare8192 {h} 100\nsquare8192/w4 {hq} 200\nsquare8192/nf4 {h} 250\n"
+        f"skinny {h[::-1]} 300\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "kernel_source_hash", lambda: h)
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda dequant=False: hq if dequant else h)
     assert bench.traffic_from_profiles("square8192") == 100.0
     assert bench.traffic_from_profiles("square8192/w4") == 200.0
+    assert bench.traffic_from_profiles("square8192/nf4") is None  # recorded with the dense hash
     assert bench.traffic_from_profiles("skinny") is None  # taken on another source
 
 
