@@ -415,6 +415,12 @@ def other_workloads(args, headline, lib, binding, dev, stream, bus, peaks, peak_
         }
         if clocks.get("sm_mhz"):
             entry["sm_cycles_per_step"] = ms * 1e-3 * clocks["sm_mhz"] * 1e6
+        if roof["bound"] == "tensor" and "bf16_tflops_sustained" in peaks:
+            # each workload is timed for about half a second of back-to-back steps, the regime
+            # of the seconds-long cuBLAS loop behind the sustained peak: reported beside frac
+            sus = peaks["bf16_tflops_sustained"] * FP16_OVER_BF16
+            entry["roofline"]["peak_sustained"] = sus
+            entry["roofline"]["frac_of_sustained"] = roof["achieved"] / sus
         if plan["kernels"] > 1:
             entry["note"] = ("frac is the whole step (operand repack, GEMM and split-K "
                              "reduction) against the GEMM's roofline")
