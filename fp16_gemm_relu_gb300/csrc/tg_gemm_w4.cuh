@@ -790,6 +790,9 @@ constexpr int kW4TDeqWarps = kW4TDeqGroups * kW4TGroupWarps;
 constexpr int kW4TMma2Warp = 2 + kEpiWarps + kW4TDeqWarps;  // second MMA issuer
 constexpr int kW4TThreads = (3 + kEpiWarps + kW4TDeqWarps) * 32;
 
+// activation(x, act) kept out of line, for the GELU forms in unrolled epilogue loops.
+__device__ __noinline__ float activation_outlined(float x, int act) { return activation(x, act); }
+
 // TDEC: the dequantisers write the decoded tile into tensor memory instead of shared memory,
 // and the MMA reads its A operand (the decoded weights) from there.  Each dequantiser thread
 // owns one TMEM lane = one output column of the tile and writes that column's 64 weights of a
@@ -1021,14 +1024,21 @@ __global__ void __launch_bounds__(kW4TThreads, 1)
       const bool n_ok = n < p.N;
       const float bias = (n_ok && p.bias) ? __half2float(p.bias[n]) : 0.0f;
       unsigned short* cp = reinterpret_cast<unsigned short*>(p.c);
-      // rows m0 .. m0 + 31 of column n, from 32 float32 sums
+      // rows m0 .. m0 + 31 of column n, from 32 float32 sums.  The GELU forms go through one
+      // out-of-line copy of the activation: with the activation switch inlined in all 32
+      // unrolled rows, the kernel's end (its TMEM release) took ~5 us longer on the
+      // decode-like shapes, though those paths never ran.
       auto store_rows = [&](const uint32_t (&r)[32], int m0) {
         if (!n_ok) return;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int m = m0 + j;
           if (m < p.M) {
-            float x = activation(__uint_as_float(r[j]) + bias, p.act);
+            float x = __uint_as_float(r[j]) + bias;
+            if (p.act == kActRelu)
+              x = x > 0.0f ? x : 0.0f;  // as activation(x, kActRelu)
+            else if (p.act != kActNone)
+              x = activation_outlined(x, p.act);
             if (p.residual) x += __half2float(p.residual[static_cast<long long>(m) * p.ldr + n]);
             cp[static_cast<long long>(m) * p.ldc + n] = __half_as_ushort(__float2half_rn(x));
           }
