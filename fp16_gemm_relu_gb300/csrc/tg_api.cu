@@ -18,7 +18,11 @@
 namespace {
 
 constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1024;  // TMA coordinates are 32-bit
-constexpr int kDefaultPanel = 16;
+// L2 panel height in M-tiles (units walk the M-tiles of a panel fastest).  Measured against 16,
+// best of two runs with L2 flushed: 2048^3 20.4 against 21.4 us, 5000x4000x1000 49.3 against
+// 51.2 us, ragged 4095x3073x65537 1.320 against 1.331 ms, 8192^3 and 64x28672x8192 unchanged;
+// 8192^3 reads 1.05 GB of DRAM per launch against 1.26 GB (4 and 32 are slower and read more).
+constexpr int kDefaultPanel = 8;
 constexpr int kDefaultTimeoutMs = 2000;
 constexpr int kBlockNs[3] = {256, 192, 128};
 constexpr int kMaxOverlapSplits = 32;  // the plan's largest split count
