@@ -33,6 +33,7 @@ from fp16_gemm_relu_gb300 import workloads  # noqa: E402
 METRIC = "GEMM+ReLU TFLOP/s (2MNK/t) and % of GB300 fp16 tensor/HBM roofline, 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_FIRST_MIN_M = 768  # the int4/NF4 GEMM's default: decode the weights first from this M
 FP16_OVER_BF16 = 1.0  # dense fp16 and bf16 tensor rates are equal (nominal 2.25 PF each)
 
 
@@ -473,9 +474,13 @@ def run_ours(args, wl):
                                                   1.0 / np.sqrt(wl.K))).to(dev)
         del B
         alg_bytes = 2 * wl.M * wl.K + wl.K * wl.N // 2 + 2 * wl.N * (-(-wl.K // G)) + 2 * wl.M * wl.N
-        # the int4 kernel the library picks for the two int4 workloads: the swapped-operand
-        # kernel for a few rows of A, 256 x 256 CTA-pair tiles for many
-        if wl.M <= 128:
+        # the int4 plan the library picks for the two int4 workloads: the swapped-operand
+        # kernel for a few rows of A; for many (M >= 768, the library's default threshold)
+        # the weights decoded once into fp16 scratch, then the fp16 GEMM
+        if wl.M >= DECODE_FIRST_MIN_M:
+            plan = {"block_m": 256, "block_n": 256, "block_k": 64, "kernels": 2,
+                    "kernel": "tg_dequant_kernel (weights to fp16 scratch), then the fp16 GEMM"}
+        elif wl.M <= 128:
             # the library's rule for the swapped kernel: a last wave of at most half a grid
             # of tiles runs as two K halves
             bmt = 64 if wl.M <= 64 else 128
@@ -487,7 +492,8 @@ def run_ours(args, wl):
         else:
             plan = {"block_m": 256, "block_n": 256, "block_k": 64,
                     "kernel": "tg_gemm_w4_pair_kernel"}
-        plan.update({"split_k": 1, "kernels": 1, "dequant": f"{args.dequant} g128"})
+        plan.setdefault("kernels", 1)
+        plan.update({"split_k": 1, "dequant": f"{args.dequant} g128"})
         dq_fn = lib.tg_gemm_w4a16_f16 if args.dequant == "w4" else lib.tg_gemm_nf4a16_f16
 
         def step():

@@ -31,7 +31,7 @@ class tg_options(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "block_n", "split_k", "force_repack", "force_workspace", "panel_m", "max_ctas",
         "debug_flags", "timeout_ms", "pair", "tail", "swap_ab", "a_in_place",
-        "repack_overlap", "tmem_decode")]
+        "repack_overlap", "tmem_decode", "dequant_first")]
 
 
 class tg_epilogue(ctypes.Structure):

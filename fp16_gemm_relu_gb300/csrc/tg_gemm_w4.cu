@@ -8,6 +8,12 @@
 
 namespace {
 
+// Smallest M for which the decode-first plan is chosen by default.  On GB300 (int4 / NF4,
+// L2 flushed): N = K = 8192 fused against decode-first at M = 512 92 / 104 us, M = 768
+// 166 / 142 us, M = 8192 1028 / 660 us; N = K = 4096 at M = 1024 51 / 47 us.
+constexpr int64_t kDecodeFirstMinM = 768;
+
+
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <int BMT, int FMT, bool TDEC = false>
@@ -132,7 +138,7 @@ tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C
   if (o.block_n != 0 && o.block_n != 128 && o.block_n != 256) return TG_ERR_INVALID_ARG;
   if (o.max_ctas < 0 || o.panel_m < 0 || o.timeout_ms < 0 || o.swap_ab < -1 || o.swap_ab > 1 ||
       o.pair < -1 || o.pair > 1 || o.tail < -1 || o.tail > 1 || o.tmem_decode < 0 ||
-      o.tmem_decode > 1)
+      o.tmem_decode > 1 || o.dequant_first < -1 || o.dequant_first > 1)
     return TG_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return TG_OK;
   if (C == nullptr) return TG_ERR_INVALID_ARG;
@@ -151,6 +157,42 @@ tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C
   if (st != TG_OK) return st;
   PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   if (!tg::tensor_map_encoder(&enc)) return tg::record_cuda_error(cudaErrorNotSupported);
+
+  // Decode first: for large M the GEMM is compute-bound, and one pass that writes the weights
+  // as fp16 (K x N x 2 bytes) costs less than decoding every weight tile inside the GEMM.
+  const bool fused_override = o.swap_ab != 0 || o.pair != 0 || o.block_n != 0 ||
+                              o.tmem_decode != 0;
+  if (o.dequant_first > 0 || (o.dequant_first == 0 && !fused_override && M >= kDecodeFirstMinM)) {
+    const int64_t ldw = (N + 7) / 8 * 8;
+    void* w16 = nullptr;
+    st = tg::scratch_alloc(size_t(K) * size_t(ldw) * 2, stream, &w16);
+    if (st != TG_OK && o.dequant_first > 0) return st;
+    if (st == TG_OK) {
+      const int64_t words = cdiv(N, 8);
+      const dim3 grid(static_cast<unsigned>(cdiv(words, 256)),
+                      static_cast<unsigned>(std::min<int64_t>(K, 65535)));
+      tg::tg_dequant_kernel<FMT><<<grid, 256, 0, stream>>>(
+          static_cast<const uint32_t*>(Wq), ldq, static_cast<const uint16_t*>(scales), lds,
+          group_size, K, N, static_cast<uint16_t*>(w16), ldw);
+      const cudaError_t ce = cudaGetLastError();
+      if (ce == cudaSuccess) {
+        tg_options go;  // the options the fp16 GEMM knows; the int4-kernel ones do not apply
+        std::memset(&go, 0, sizeof(go));
+        go.max_ctas = o.max_ctas;
+        go.panel_m = o.panel_m;
+        go.tail = o.tail;
+        go.timeout_ms = o.timeout_ms;
+        go.debug_flags = o.debug_flags;
+        st = tg_gemm_f16_epilogue(A, w16, C, M, N, K, lda, ldw, ldc, &e, &go, stream_);
+      } else {
+        st = tg::record_cuda_error(ce);
+      }
+      const cudaError_t fe = cudaFreeAsync(w16, stream);
+      if (st == TG_OK && fe != cudaSuccess) st = tg::record_cuda_error(fe);
+      return st;
+    }
+    st = TG_OK;  // no scratch: the fused kernels need none for most plans
+  }
 
   const int grid_cap0 = o.max_ctas > 0 ? std::min(o.max_ctas, sms) : sms;
   const bool swap = o.swap_ab > 0 || (o.swap_ab == 0 && M <= 128);

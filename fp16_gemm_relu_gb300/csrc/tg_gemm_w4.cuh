@@ -224,6 +224,67 @@ __device__ __forceinline__ uint4 decode8(uint32_t w, const uint32_t (&sp)[4]) {
   }
 }
 
+// Eight int4 weights of one packed word in column order: pr[j] holds columns (2j, 2j+1), sv the
+// eight columns' fp16 scales in the same order.  The arithmetic of dequant8 per weight:
+// (1024 + q) - 1032 = q - 8 exactly, then one rounding in the product with the scale.
+__device__ __forceinline__ uint4 dequant8_in_order(uint32_t w, const uint4& sv) {
+  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const uint32_t s[4] = {sv.x, sv.y, sv.z, sv.w};
+  uint32_t pr[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t t = w >> (8 * j);  // columns 2j and 2j+1 in bits [0, 4) and [4, 8)
+    const uint32_t x = (t & 0xFu) | ((t & 0xF0u) << 12) | 0x64006400u;
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), k1032);
+    h = __hmul2(h, *reinterpret_cast<const __half2*>(&s[j]));
+    pr[j] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return make_uint4(pr[0], pr[1], pr[2], pr[3]);
+}
+
+// The whole weight matrix decoded to fp16, for the decode-first plan of large M: w16[k][n] is
+// the weight of row k, column n (K rows of ldw >= N rounded up to 8 values), the same values
+// the fused kernels feed their MMAs; the columns of the last word past N are written as +0.
+// Thread x of block (bx, by) takes word column c = bx * 256 + x of rows by, by + gridDim.y, ...
+template <int FMT>
+__global__ void __launch_bounds__(256)
+    tg_dequant_kernel(const uint32_t* __restrict__ wq, int64_t ldq,
+                      const uint16_t* __restrict__ scales, int64_t lds, int group_size,
+                      int64_t K, int64_t N, uint16_t* __restrict__ w16, int64_t ldw) {
+  const int64_t words = (N + 7) / 8;
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= words) return;
+  const bool whole = 8 * c + 8 <= N;
+  for (int64_t k = blockIdx.y; k < K; k += gridDim.y) {
+    const uint32_t w = __ldg(wq + k * ldq + c);
+    const uint16_t* srow = scales + (k / group_size) * lds + 8 * c;
+    uint4 sv;
+    if (whole) {
+      sv = __ldg(reinterpret_cast<const uint4*>(srow));
+    } else {
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = 8 * c + 2 * j < N ? __ldg(srow + 2 * j) : 0u;
+        const uint32_t hi = 8 * c + 2 * j + 1 < N ? __ldg(srow + 2 * j + 1) : 0u;
+        h[j] = lo | (hi << 16);
+      }
+      sv = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    uint4 v = FMT == kFmtInt4 ? dequant8_in_order(w, sv) : dequant8_nf4(w, sv);
+    if (!whole) {  // columns past N: +0
+      uint32_t o[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (8 * c + 2 * j >= N) o[j] &= 0xFFFF0000u;
+        if (8 * c + 2 * j + 1 >= N) o[j] &= 0x0000FFFFu;
+      }
+      v = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    *reinterpret_cast<uint4*>(w16 + k * ldw + 8 * c) = v;
+  }
+}
+
 // tmA: fp16 A {K, M} box {64, 128} SW128; tmQ: uint32 Wq {ceil(N/8), K} box {BN/8, 64};
 // tmS: fp16 scales {N, ceil(K/G)} box {BN, 1}; tmOut: fp16 C {n_tma, M} box {64, 32} SW128.
 // p.splits must be 1; p.kb_per_split = p.num_kb; p.group_kb = G / 64.

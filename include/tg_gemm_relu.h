@@ -117,6 +117,11 @@ typedef struct {
                            its column's nibbles row by row: slower than the default on every
                            shape measured, e.g. 64 x 28672 x 8192 int4 111 against 93 us);
                            0 decode into shared memory */
+  int dequant_first;    /* int4 / NF4 GEMM: 1 decode the whole weight matrix once into fp16
+                           scratch (K x N rounded up to 8, 2 bytes each, from the library's
+                           pool) and run the fp16 GEMM on it; -1 never; 0 choose: decode first
+                           when M is large enough (see tg_gemm_w4a16_f16) and no other
+                           int4-kernel override (swap_ab, pair, block_n, tmem_decode) is set */
 } tg_options;
 
 /* Fault injection: the first producer of the grid drops its first stage (no load, no
@@ -207,7 +212,12 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
  * scales: device fp16, ceil(K/G) rows of lds values (lds >= N, multiple of 8, 16-byte
  *     aligned).  group_size G: a multiple of 64.
  * C: device fp16 M x N, 16-byte aligned, ldc a multiple of 8.  epi as tg_gemm_f16_epilogue.
- * The weights are decoded inside the GEMM kernel (never written to memory).  Kernels: for
+ * Plans: by default for M >= 768 with no int4-kernel override (opt->dequant_first), the whole
+ * weight matrix is decoded once into fp16 scratch from the library's pool (K x N rounded up to
+ * 8, 2 bytes each; released in stream order), the same values the fused kernels use, and the
+ * fp16 GEMM (tg_gemm_f16_epilogue) runs on it; without scratch the plan falls back to a fused
+ * kernel (TG_ERR_NO_WORKSPACE only when dequant_first = 1 forces it).  Otherwise the weights are
+ * decoded inside the GEMM kernel (never written to memory).  Fused kernels: for
  * M <= 128 the swapped-operand kernel (C^T = W^T A^T; opt->swap_ab); otherwise, by default for
  * M >= 256 when the 256 x 256 tiles fill at least half of the clusters of two CTAs that fit at
  * once, 256 x 256 tiles on CTA pairs, each CTA decoding half of the weight tile (opt->pair:

@@ -184,7 +184,8 @@ def test_w4_argument_errors(lib):
     assert call((4, 0)) == binding.TG_OK                    # M == 0
     # plan options out of range are rejected before any device work
     for opts in ({"pair": 2}, {"pair": -2}, {"tail": 2}, {"tail": -2}, {"swap_ab": 3},
-                 {"block_n": 192}, {"max_ctas": -1}):
+                 {"block_n": 192}, {"max_ctas": -1}, {"dequant_first": 2},
+                 {"dequant_first": -2}):
         assert binding.tg_gemm_w4a16_f16(p, p, p, p, 64, 64, 64, 64, 8, 64, 64, 128,
                                          options=opts) == binding.TG_ERR_INVALID_ARG, opts
 

@@ -24,7 +24,8 @@ def test_nf4_every_code_value():
     base = np.array([0x76543210, 0xFEDCBA98, 0x13579BDF, 0x02468ACE], np.uint32)
     Wq = np.ascontiguousarray(np.stack([np.roll(base, r) for r in range(K)])[:, np.arange(16) % 4])
     S = inputs.int4_scales(1, N, 5, 0.5, lds=N)
-    for opts in ({"swap_ab": 1}, {"swap_ab": -1, "block_n": 128}, {"swap_ab": -1, "pair": 1}):
+    for opts in ({"swap_ab": 1}, {"swap_ab": -1, "block_n": 128}, {"swap_ab": -1, "pair": 1},
+                 {"dequant_first": 1}):
         got = run_w4(a, Wq, S, N, G, options=opts, fmt="nf4")
         check(got, a, Wq, S, N, G, fmt="nf4")
 

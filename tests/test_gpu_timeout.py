@@ -60,7 +60,8 @@ def test_host_entry_reports_clean_status():
 
 
 @pytest.mark.parametrize("fmt", ["int4", "nf4"])
-@pytest.mark.parametrize("kernel", ["swapped", "swapped_tmem", "single_cta", "cta_pair"])
+@pytest.mark.parametrize("kernel", ["swapped", "swapped_tmem", "single_cta", "cta_pair",
+                                    "decode_first"])
 def test_dequant_kernels_dropped_stage_times_out(fmt, kernel):
     # the same injected fault in the three dequantising GEMM kernels: their waits are bounded
     # like the fp16 kernels'; after the timeout the next call on the context is correct
@@ -74,7 +75,9 @@ def test_dequant_kernels_dropped_stage_times_out(fmt, kernel):
     # "swapped_tmem": 64 rows of A, weights decoded into tensor memory on request
     M, N, K, G = (64 if kernel == "swapped_tmem" else 256), 512, 2048, 128
     a, Wq, S = make(M, N, K, G, 41)
+    # "decode_first": the fp16 GEMM after the decode pass takes the injected fault
     base = {"swapped": {"swap_ab": 1}, "swapped_tmem": {"swap_ab": 1, "tmem_decode": 1},
+            "decode_first": {"dequant_first": 1},
             "single_cta": {"swap_ab": -1, "block_n": 128},
             "cta_pair": {"swap_ab": -1, "pair": 1}}[kernel]
     opts = dict(base, debug_flags=binding.TG_DEBUG_DROP_FIRST_STAGE, timeout_ms=200)

@@ -123,9 +123,9 @@ def test_w4_decode_shape_sampled():
 
 
 def test_w4_square_workload_sampled():
-    # the int4 bench workload at full size in its default launch (the CTA-pair kernel):
-    # square8192's A, weights and scales as the bench makes them, sampled rows and columns
-    # across tile and cluster boundaries
+    # the int4 bench workload at full size: square8192's A, weights and scales as the bench
+    # makes them, sampled rows and columns across tile and cluster boundaries, in the default
+    # launch (decode first, then the fp16 GEMM) and with the fused CTA-pair kernel
     from fp16_gemm_relu_gb300 import workloads
 
     wl = workloads.get("square8192")
@@ -133,12 +133,45 @@ def test_w4_square_workload_sampled():
     a = wl.make_a()
     Wq = inputs.int4_weights(K, N, wl.seed)
     S = inputs.int4_scales(K // G, N, wl.seed, 1.0 / np.sqrt(K))
-    got = run_w4(a, Wq, S, N, G, act=1)
     rng = np.random.default_rng(1)
     rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], rng.integers(0, M, 40)]))
     cols = np.unique(np.concatenate([[0, 7, 8, 127, 128, 255, 256, N - 1],
                                      rng.integers(0, N, 40)]))
-    check(got[np.ix_(rows, cols)], a, Wq, S, N, G, "relu", rows=rows, cols=cols)
+    for opts in (None, {"pair": 1}):
+        got = run_w4(a, Wq, S, N, G, act=1, options=opts)
+        check(got[np.ix_(rows, cols)], a, Wq, S, N, G, "relu", rows=rows, cols=cols)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nf4"])
+@pytest.mark.parametrize("M,N,K,G", [(1, 257, 640, 128), (300, 527, 1030, 128), (800, 1000, 640, 192),
+                                     (129, 1301, 1537, 64)])
+@pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
+def test_decode_first(fmt, M, N, K, G, act):
+    # the whole weight matrix decoded to fp16 scratch, then the fp16 GEMM: ragged N (the last
+    # packed word's columns past N), partial scale groups, fused epilogues
+    a, Wq, S = make(M, N, K, G, 41)
+    ACT = {"relu": 1, "gelu_tanh": 3}
+    bias = inputs.tensor(1, N, 42, 0).ravel()
+    res = inputs.tensor(M, N, 42, 1)
+    got = run_w4(a, Wq, S, N, G, act=ACT[act], bias=bias, residual=res,
+                 options={"dequant_first": 1}, fmt=fmt)
+    check(got, a, Wq, S, N, G, act, bias, res, fmt=fmt)
+    got0 = run_w4(a, Wq, S, N, G, act=1, options={"dequant_first": 1, "max_ctas": 3}, fmt=fmt)
+    check(got0, a, Wq, S, N, G, "relu", fmt=fmt)
+
+
+@pytest.mark.parametrize("fmt", ["int4", "nf4"])
+def test_decode_first_is_the_default_for_large_m(fmt):
+    # with no kernel override, M >= 768 takes the decode-first plan: bitwise what forcing it
+    # gives (each plan is deterministic)
+    M, N, K, G = 1024, 768, 2048, 128
+    a, Wq, S = make(M, N, K, G, 43)
+    auto = run_w4(a, Wq, S, N, G, act=1, fmt=fmt)
+    forced = run_w4(a, Wq, S, N, G, act=1, options={"dequant_first": 1}, fmt=fmt)
+    np.testing.assert_array_equal(auto, forced)
+    check(auto, a, Wq, S, N, G, "relu", fmt=fmt)
+    fused = run_w4(a, Wq, S, N, G, act=1, options={"dequant_first": -1}, fmt=fmt)
+    check(fused, a, Wq, S, N, G, "relu", fmt=fmt)
 
 
 @pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
