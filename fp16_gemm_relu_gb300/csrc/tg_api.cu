@@ -1180,6 +1180,6 @@ tg_status tg_release_workspace(void) {
   return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }
 
-int tg_version(void) { return 200; }
+int tg_version(void) { return 300; }
 
 }  // extern "C"

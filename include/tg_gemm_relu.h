@@ -318,7 +318,8 @@ tg_status tg_gemm_relu_f16_splitk_noalloc(const void* A, const void* B, void* C,
                                           int64_t ldc, int epilogue_flag, int split_k,
                                           tg_stream_t stream);
 
-/* Library version as major*10000 + minor*100 + patch. */
+/* Library version as major*10000 + minor*100 + patch.  300: tg_options gained dequant_first
+ * (callers must be built against this header). */
 int tg_version(void);
 
 #ifdef __cplusplus

@@ -42,7 +42,7 @@ def test_status_strings(lib):
     for s in range(7):
         assert binding.tg_status_string(s)
     assert binding.tg_status_string(99) == "unknown status"
-    assert binding.tg_version() == 200
+    assert binding.tg_version() == 300
 
 
 def test_validation_before_any_device_work(lib):
