@@ -48,8 +48,8 @@ def parse_args():
                     help="backward: one step = dZ = relu'(C) * dC, dA = dZ B^T, dB = A^T dZ "
                          "(4MNK flops), all in the library's kernels")
     ap.add_argument("--dequant", default="none", choices=["none", "w4", "nf4"],
-                    help="w4 / nf4: B is int4 / NF4 weights (group 128 scales) decoded inside "
-                         "the GEMM")
+                    help="w4 / nf4: B is int4 / NF4 weights (group 128 scales), decoded inside "
+                         "the GEMM (or, for M >= 768, once into fp16 before the fp16 GEMM)")
     ap.add_argument("--epilogue", default="relu", choices=["relu", "bias_gelu", "bias_relu_residual"],
                     help="relu: the metric's path; the others time the fused bias/GELU/residual "
                          "epilogue on the same GEMM")
