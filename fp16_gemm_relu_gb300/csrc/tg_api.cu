@@ -195,9 +195,10 @@ double kblock_cycles(int bn) {
 }
 
 // Plan selection (host only): tries every tile width and split count and keeps the fastest
-// by a simple model.  Compute time = waves x k-blocks per unit x kblock_cycles / 1.9 GHz;
-// memory time = the algorithmic bytes at 6.8 TB/s, inflated when a wave keeps fewer than
-// 60% of the SMs busy; plus the float32 workspace traffic of split-K and its extra launch.
+// by a simple model.  Compute time = waves x k-blocks per unit x kblock_cycles / 1.9 GHz
+// (a tail-split last wave counts half); memory time = the algorithmic bytes at 6.8 TB/s,
+// inflated when a wave keeps fewer than 60% of the SMs busy; plus the float32 workspace
+// traffic of split-K and its extra launch, and the operand copies of unaligned operands.
 tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N, int64_t K,
                     int64_t lda, int64_t ldb, int64_t ldc, int num_sms, int pair_clusters,
                     const tg_options* opt, Plan* out, int ta = 0, int tb = 0) {
@@ -235,6 +236,14 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
   const int grid_cap = o.max_ctas > 0 ? std::min(o.max_ctas, num_sms) : num_sms;
   const double clk = 1.9e9, hbm = 6.8e12;
   const double alg_bytes = 2.0 * (double(M) * K + double(K) * N + double(M) * N);
+  // Operand copies (each element read once, written once).  Made first, they add their full
+  // time.  Overlapped split by split (split-K only), the first split's copy runs alone and the
+  // others still cost ~3/4 of their time, since they share DRAM and L2 with the GEMMs; every
+  // further split also adds a launch and two copies (~5 us).  Calibrated on unaligned shapes
+  // from 1 x 4096 x 8192 to 4095 x 3073 x 65537, timed with each plan forced.
+  const double copy_time = 4.0 * ((P.repack_a ? double(M) * K : 0.0) +
+                                  (P.repack_b ? double(K) * N : 0.0)) / hbm;
+  const bool may_overlap = copy_time > 0.0 && o.repack_overlap >= 0 && o.a_in_place == 0;
 
   struct Cand {
     double t;
@@ -265,23 +274,33 @@ tg_status make_plan(uintptr_t a, uintptr_t b, uintptr_t c, int64_t M, int64_t N,
       // time alone (each SM loads 32 KB per k-block, well under the L2 budget)
       const int64_t slots_cap = pair ? pair_cap : grid_cap;
       const int64_t grid = std::min<int64_t>(units, slots_cap);
-      const int64_t waves = cdiv(units, grid);
       const bool ws = s_eff > 1 || !c_direct;
+      // the pair kernel's tail split (below) runs a last wave of at most half the clusters as
+      // K halves on twice as many clusters, in half a wave's time
+      const bool tail = pair && s_eff == 1 && !ws && o.tail >= 0 && P.kblocks >= 2 &&
+                        units > grid && units % grid != 0 && 2 * (units % grid) <= grid;
+      const double waves = tail ? double(units / grid) + 0.5 : double(cdiv(units, grid));
       const double kb_cycles = pair ? 512.0 : kblock_cycles(bn);
       // the pair kernel's cluster launch and its first 64 KB stage per CTA cost ~2 us more
       // before the first MMA than the single-CTA kernel's start (measured on 2048^3, one wave
       // either way: 22.6 us against 20.5 us)
       const double t_start = pair ? 2.1e-6 : 0.0;
-      const double t_mma = double(waves) * double(kbps) * kb_cycles / clk + t_start;
+      // the tail's K halves meet through a float32 workspace: ~5 us, which short K does not win
+      // back
+      const double t_mma = waves * double(kbps) * kb_cycles / clk + t_start + (tail ? 5e-6 : 0.0);
+      const bool overlap = may_overlap && s_eff >= 2 && s_eff <= kMaxOverlapSplits;
+      const double t_copy =
+          overlap ? copy_time * (1.0 / s_eff + 0.75 * (1.0 - 1.0 / s_eff)) + (s_eff - 1) * 5e-6
+                  : copy_time;
       double slots = 0.0;  // wave-by-wave occupancy penalty on the memory time
-      for (int64_t wv = 0; wv < waves; ++wv) {
+      for (int64_t wv = 0; wv < cdiv(units, grid); ++wv) {
         const int64_t active = (pair ? 2 : 1) * std::min<int64_t>(grid, units - wv * grid);
         slots += std::max<double>(double(active), 0.6 * num_sms);
       }
       const double t_hbm = alg_bytes / hbm * (slots / double((pair ? 2 : 1) * units));
       // workspace traffic plus the extra launch of the reduction kernel (~3 us)
       const double t_ws = ws ? (2.0 * 4.0 * double(s_eff) * M * N + 2.0 * M * N) / hbm + 3e-6 : 0.0;
-      cands[nc++] = Cand{std::max(t_mma, t_hbm) + t_ws, bn, static_cast<int>(s_eff),
+      cands[nc++] = Cand{std::max(t_mma, t_hbm) + t_ws + t_copy, bn, static_cast<int>(s_eff),
                          static_cast<int>((pair ? 2 : 1) * grid), pair};
     }
   }

@@ -93,6 +93,32 @@ def test_plan_pair_overrides(lib):
     assert st == binding.TG_ERR_INVALID_ARG
 
 
+def test_plan_short_k_keeps_single_cta_tiles(lib):
+    # at K <= 1024 the pair kernel's start and its tail split cost more than they save: on
+    # GB300 8192x8192x512 ran 76.8 us on 128x256 tiles against 96.1 us on pair tiles
+    for M, N, K in [(8192, 8192, 256), (8192, 8192, 512), (4096, 4096, 1024)]:
+        p = _plan(M, N, K)
+        assert p["cta_pair"] == 0 and p["split_k"] == 1, (M, N, K, p)
+
+
+def test_plan_long_k_prefers_the_tail_split_over_split_k(lib):
+    # aligned C and a last wave of at most half the clusters: one K pass with the tail split
+    # beats two or three K splits through the workspace (2048x8192x65536: 1296 against
+    # 1340 us; 12288x512x16384: 150 against 167 us)
+    for M, N, K in [(2048, 8192, 65536), (12288, 512, 16384), (2048, 3072, 16384)]:
+        p = _plan(M, N, K)
+        assert p["cta_pair"] == 1 and p["split_k"] == 1 and p["tail_tiles"] > 0, (M, N, K, p)
+
+
+def test_plan_unaligned_small_problem_few_splits(lib):
+    # an unaligned B on a small problem: every overlapped split is one more GEMM launch and two
+    # copies, so the plan keeps the split count low (1000x100x8192: 3 splits ran 57 us, the
+    # 13 of a model without that cost 126 us; 1x4096x8192: 81 against 212 us)
+    for M, N, K, lda, ldb in [(1000, 100, 8192, 8195, 103), (1, 4096, 8192, 8195, 4099)]:
+        p = _plan(M, N, K, lda=lda, ldb=ldb, ldc=N + 1)
+        assert p["repack_b"] == 1 and p["split_k"] <= 4, (M, N, K, p)
+
+
 def test_plan_skinny_fills_the_machine(lib):
     p = _plan(64, 28672, 8192)
     assert p["units"] >= 0.95 * 152 or p["split_k"] > 1

@@ -141,9 +141,9 @@ def test_workload_integer_inputs_bitwise(name):
 def test_default_tail_split_with_ragged_edges():
     # 20 x 16 = 320 pair tiles: four full waves of 76 clusters, then 16 tiles that the default
     # plan runs as 32 K halves.  M, N and K all end in partial tiles (5000 = 19*256 + 136,
-    # 4000 = 15*256 + 160, 1000 = 15*64 + 40), so the split tiles include edge tiles and the
-    # second K half ends in a partial k-block.
-    M, N, K = 5000, 4000, 1000
+    # 4000 = 15*256 + 160, 1500 = 23*64 + 28), so the split tiles include edge tiles and the
+    # second K half ends in a partial k-block.  (At K = 1000 the plan keeps 128 x 256 tiles.)
+    M, N, K = 5000, 4000, 1500
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     st, plan = binding.tg_plan_query(0x1000, 0x2000, 0x3000, M, N, K, K, N, N, sms)
     assert st == binding.TG_OK and plan["cta_pair"] == 1
