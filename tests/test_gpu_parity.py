@@ -308,3 +308,36 @@ def test_repack_overlap_matches_sequential(M, N, K, lda, ldb, split):
     bi = inputs.tensor(K, N, 82, 1, "int")
     ci, _ = run_gpu(ai, bi, True, opts, lda=lda, ldb=ldb, ldc=N + 5)
     np.testing.assert_array_equal(ci, oracle.gemm_relu(ai, bi, relu=True, want=("f32",))["out16_f32acc"])
+
+
+@pytest.mark.parametrize("M,N,K,lda,ldb,ldc,expect", [
+    # short K: the default keeps single-CTA 128 x 256 tiles
+    (4096, 4096, 512, 512, 4096, 4096, {"cta_pair": 0, "split_k": 1}),
+    # long K, aligned C, a last wave of at most half the clusters: one K pass, tail split
+    (2048, 3072, 16384, 16384, 3072, 3072, {"cta_pair": 1, "split_k": 1, "tail": True}),
+    # unaligned strides on small problems: a few overlapped splits, not 13 to 32
+    (1000, 100, 8192, 8195, 103, 101, {"repack_b": 1, "max_split": 4}),
+    (1, 4096, 8192, 8195, 4099, 4097, {"repack_b": 1, "max_split": 4}),
+])
+def test_cost_model_defaults_parity(M, N, K, lda, ldb, ldc, expect):
+    # the plans the cost model picks for these shape classes (pinned on the host side too),
+    # run by default and compared with the oracle over every output; integer inputs bit for bit
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, plan = binding.tg_plan_query(0x100000, 0x200000, 0x300000, M, N, K, lda, ldb, ldc, sms)
+    assert st == binding.TG_OK
+    for k in ("cta_pair", "split_k", "repack_b"):
+        if k in expect:
+            assert plan[k] == expect[k], (k, plan)
+    if expect.get("tail"):
+        assert plan["tail_tiles"] > 0, plan
+    if "max_split" in expect:
+        assert 1 <= plan["split_k"] <= expect["max_split"], plan
+    a = inputs.tensor(M, K, 97, 0)
+    b = inputs.tensor(K, N, 97, 1)
+    c, pad_ok = run_gpu(a, b, True, None, lda=lda, ldb=ldb, ldc=ldc)
+    assert pad_ok
+    assert_parity(c, oracle_ref(a, b, True), K, True, where=f"default plan {M}x{N}x{K}")
+    ai = inputs.tensor(M, K, 98, 0, "int")
+    bi = inputs.tensor(K, N, 98, 1, "int")
+    ci, _ = run_gpu(ai, bi, True, None, lda=lda, ldb=ldb, ldc=ldc)
+    np.testing.assert_array_equal(ci, oracle.gemm_relu(ai, bi, relu=True, want=("f32",))["out16_f32acc"])
