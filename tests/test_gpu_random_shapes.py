@@ -6,7 +6,8 @@ tests/parity.py. The draws cover:
   - relu(A·B) with unaligned leading dimensions and 2-byte-aligned base pointers (the copy paths)
     and with aligned ones (single-CTA, CTA-pair, split-K and tail-split plans);
   - the fused bias / activation / residual epilogue with padded ldc;
-  - the int4 and NF4 weight GEMMs with groups of 64 to 256 rows.
+  - the int4 and NF4 weight GEMMs with groups of 64 to 256 rows;
+  - the transposed-operand GEMM with every combination of stored layouts.
 C's padding must come back untouched. Every case is its own test id, so a failure names its
 shape."""
 
@@ -139,3 +140,26 @@ def test_weight_gemm_random(fmt, i):
     res = compare(got[rows], {"out16_f64acc": r["out16_f64acc"], "acc_f64": r["pre_f64"]}, K,
                   relu=act == "relu")
     _assert_ok(res, act == "relu", f"{fmt} {M}x{N}x{K} G={G} {act}")
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_transposed_random(i):
+    # tg_gemm_f16_t with A and/or B stored transposed (the backward GEMMs' layouts), padded or
+    # unaligned leading dimensions, no activation
+    from tests.test_gpu_backward import gemm_t
+
+    rng = random.Random(9500 + i)
+    while True:
+        M, N, K = _logu(rng, 1, 4096), _logu(rng, 1, 4096), _logu(rng, 1, 16384)
+        if M * K <= 3e7 and K * N <= 3e7 and M * N <= 3e7:
+            break
+    ta, tb = i & 1, (i >> 1) & 1
+    pad = rng.choice([0, 0, 3, 8])
+    a = inputs.tensor(M, K, 9500 + i, 0)
+    b = inputs.tensor(K, N, 9500 + i, 1)
+    a_st = np.ascontiguousarray(a.T) if ta else a
+    b_st = np.ascontiguousarray(b.T) if tb else b
+    got = gemm_t(a_st, b_st, ta, tb, M, N, K, None, pad=pad)
+    rows = _rows(rng, M)
+    _assert_ok(compare(got[rows], oracle.gemm_relu(a, b, relu=False, rows=rows), K, False), False,
+               f"ta={ta} tb={tb} {M}x{N}x{K} pad={pad}")
