@@ -170,7 +170,7 @@ tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C
     if (st == TG_OK) {
       const int64_t words = cdiv(N, 8);
       const dim3 grid(static_cast<unsigned>(cdiv(words, 256)),
-                      static_cast<unsigned>(std::min<int64_t>(K, 65535)));
+                      static_cast<unsigned>(std::min<int64_t>(cdiv(K, tg::kDequantRows), 65535)));
       tg::tg_dequant_kernel<FMT><<<grid, 256, 0, stream>>>(
           static_cast<const uint32_t*>(Wq), ldq, static_cast<const uint16_t*>(scales), lds,
           group_size, K, N, static_cast<uint16_t*>(w16), ldw);

@@ -245,19 +245,29 @@ __device__ __forceinline__ uint4 dequant8_in_order(uint32_t w, const uint4& sv) 
 // The whole weight matrix decoded to fp16, for the decode-first plan of large M: w16[k][n] is
 // the weight of row k, column n (K rows of ldw >= N rounded up to 8 values), the same values
 // the fused kernels feed their MMAs; the columns of the last word past N are written as +0.
-// Thread x of block (bx, by) takes word column c = bx * 256 + x of rows by, by + gridDim.y, ...
+// Thread x of block (bx, by) takes word column c = bx * 256 + x of the row chunks by,
+// by + gridDim.y, ... of kDequantRows rows each.  A chunk's loads are all issued before its
+// first store, so each thread keeps that many DRAM reads in flight (one row per thread left
+// the pass latency-bound: 43.5 us, 3.9 TB/s, on 8192 x 8192).  A chunk starts at a multiple of
+// kDequantRows and the group size is a multiple of 64, so a chunk's rows share one scale row.
+constexpr int kDequantRows = 8;
+
 template <int FMT>
 __global__ void __launch_bounds__(256)
     tg_dequant_kernel(const uint32_t* __restrict__ wq, int64_t ldq,
                       const uint16_t* __restrict__ scales, int64_t lds, int group_size,
                       int64_t K, int64_t N, uint16_t* __restrict__ w16, int64_t ldw) {
+  constexpr int R = kDequantRows;
   const int64_t words = (N + 7) / 8;
   const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (c >= words) return;
   const bool whole = 8 * c + 8 <= N;
-  for (int64_t k = blockIdx.y; k < K; k += gridDim.y) {
-    const uint32_t w = __ldg(wq + k * ldq + c);
-    const uint16_t* srow = scales + (k / group_size) * lds + 8 * c;
+  for (int64_t k0 = static_cast<int64_t>(blockIdx.y) * R; k0 < K;
+       k0 += static_cast<int64_t>(gridDim.y) * R) {
+    uint32_t w[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) w[j] = k0 + j < K ? __ldg(wq + (k0 + j) * ldq + c) : 0u;
+    const uint16_t* srow = scales + (k0 / group_size) * lds + 8 * c;
     uint4 sv;
     if (whole) {
       sv = __ldg(reinterpret_cast<const uint4*>(srow));
@@ -271,17 +281,22 @@ __global__ void __launch_bounds__(256)
       }
       sv = make_uint4(h[0], h[1], h[2], h[3]);
     }
-    uint4 v = FMT == kFmtInt4 ? dequant8_in_order(w, sv) : dequant8_nf4(w, sv);
-    if (!whole) {  // columns past N: +0
-      uint32_t o[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (8 * c + 2 * j >= N) o[j] &= 0xFFFF0000u;
-        if (8 * c + 2 * j + 1 >= N) o[j] &= 0x0000FFFFu;
+    for (int j = 0; j < R; ++j) {
+      if (k0 + j < K) {
+        uint4 v = FMT == kFmtInt4 ? dequant8_in_order(w[j], sv) : dequant8_nf4(w[j], sv);
+        if (!whole) {  // columns past N: +0
+          uint32_t o[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (8 * c + 2 * q >= N) o[q] &= 0xFFFF0000u;
+            if (8 * c + 2 * q + 1 >= N) o[q] &= 0x0000FFFFu;
+          }
+          v = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4*>(w16 + (k0 + j) * ldw + 8 * c) = v;
       }
-      v = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    *reinterpret_cast<uint4*>(w16 + k * ldw + 8 * c) = v;
   }
 }
 
