@@ -539,19 +539,74 @@ __global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ld
 }
 
 // dZ[i, j] = C[i, j] > 0 ? dC[i, j] : +0 (the relu derivative taken on the forward output C;
-// NaN or -0 in C gives +0).  Any 2-byte alignment; one element per thread per step.
+// NaN or -0 in C gives +0).  Any 2-byte alignment: row r of the grid's y range at a time, the
+// columns spread over the x range (2-D, so no index division per element).
 __global__ void tg_relu_backward_kernel(const uint16_t* __restrict__ dC, int64_t lddc,
                                         const uint16_t* __restrict__ C, int64_t ldc,
                                         uint16_t* __restrict__ dZ, int64_t lddz, int64_t M,
                                         int64_t N) {
-  const int64_t total = M * N;
-  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = idx / N;
-    const int64_t c = idx - r * N;
-    const uint16_t cv = __ldg(C + r * ldc + c);
-    const bool pos = (cv & 0x8000u) == 0 && cv != 0 && (cv & 0x7FFFu) <= 0x7C00u;
-    dZ[r * lddz + c] = pos ? __ldg(dC + r * lddc + c) : uint16_t(0);
+  for (int64_t r = blockIdx.y; r < M; r += gridDim.y) {
+    for (int64_t c = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; c < N;
+         c += int64_t(gridDim.x) * blockDim.x) {
+      const uint16_t cv = __ldg(C + r * ldc + c);
+      const bool pos = (cv & 0x8000u) == 0 && cv != 0 && (cv & 0x7FFFu) <= 0x7C00u;
+      dZ[r * lddz + c] = pos ? __ldg(dC + r * lddc + c) : uint16_t(0);
+    }
+  }
+}
+
+// Both fp16 lanes of a 32-bit word: d's lane where c's lane is positive (sign clear, nonzero,
+// not NaN), else +0.
+__device__ __forceinline__ uint32_t relu_grad2(uint32_t c, uint32_t d) {
+  const uint32_t lo = c & 0xFFFFu, hi = c >> 16;
+  uint32_t out = 0;
+  if ((lo & 0x8000u) == 0 && lo != 0 && (lo & 0x7FFFu) <= 0x7C00u) out |= d & 0x0000FFFFu;
+  if ((hi & 0x8000u) == 0 && hi != 0 && (hi & 0x7FFFu) <= 0x7C00u) out |= d & 0xFFFF0000u;
+  return out;
+}
+
+// The same for rows that all start 16-byte aligned (the three pointers 16-byte aligned, the
+// leading dimensions multiples of 8): thread j of the x range takes 16-byte chunk j of
+// kMaskRows rows at a time, with all of their loads issued before the first store (one chunk
+// of one row per thread left the pass latency-bound); thread j == N / 8 takes the rows' last
+// N mod 8 columns one by one.
+constexpr int kMaskRows = 8;
+
+__global__ void __launch_bounds__(256)
+    tg_relu_backward_vec_kernel(const uint16_t* __restrict__ dC, int64_t lddc,
+                                const uint16_t* __restrict__ C, int64_t ldc,
+                                uint16_t* __restrict__ dZ, int64_t lddz, int64_t M, int64_t N) {
+  const int64_t chunks = N >> 3;
+  const int64_t j = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+  if (j > chunks) return;
+  for (int64_t r0 = int64_t(blockIdx.y) * kMaskRows; r0 < M;
+       r0 += int64_t(gridDim.y) * kMaskRows) {
+    if (j < chunks) {
+      uint4 cv[kMaskRows], dv[kMaskRows];
+#pragma unroll
+      for (int i = 0; i < kMaskRows; ++i) {
+        if (r0 + i < M) {
+          cv[i] = __ldg(reinterpret_cast<const uint4*>(C + (r0 + i) * ldc) + j);
+          dv[i] = __ldg(reinterpret_cast<const uint4*>(dC + (r0 + i) * lddc) + j);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kMaskRows; ++i) {
+        if (r0 + i < M) {
+          const uint4 o = make_uint4(relu_grad2(cv[i].x, dv[i].x), relu_grad2(cv[i].y, dv[i].y),
+                                     relu_grad2(cv[i].z, dv[i].z), relu_grad2(cv[i].w, dv[i].w));
+          *(reinterpret_cast<uint4*>(dZ + (r0 + i) * lddz) + j) = o;
+        }
+      }
+    } else {
+      for (int i = 0; i < kMaskRows && r0 + i < M; ++i) {
+        for (int64_t c = chunks * 8; c < N; ++c) {
+          const uint16_t cv = __ldg(C + (r0 + i) * ldc + c);
+          const bool pos = (cv & 0x8000u) == 0 && cv != 0 && (cv & 0x7FFFu) <= 0x7C00u;
+          dZ[(r0 + i) * lddz + c] = pos ? __ldg(dC + (r0 + i) * lddc + c) : uint16_t(0);
+        }
+      }
+    }
   }
 }
 
@@ -1037,10 +1092,24 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
   DeviceState* ds = nullptr;
   tg_status st = current_device(&ds);
   if (st != TG_OK) return st;
-  tg_relu_backward_kernel<<<aux_grid(M * N, ds->sm_count), 256, 0,
-                            reinterpret_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint16_t*>(dC), lddc, static_cast<const uint16_t*>(C), ldc,
-      static_cast<uint16_t*>(dZ), lddz, M, N);
+  cudaStream_t st_ = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = ((reinterpret_cast<uintptr_t>(dC) | reinterpret_cast<uintptr_t>(C) |
+                     reinterpret_cast<uintptr_t>(dZ)) & 15u) == 0 &&
+                   lddc % 8 == 0 && ldc % 8 == 0 && lddz % 8 == 0;
+  if (vec) {
+    // x: the 16-byte chunks of a row plus one thread for its last N mod 8 columns
+    const dim3 grid(static_cast<unsigned>(cdiv(N / 8 + 1, 256)),
+                    static_cast<unsigned>(std::min<int64_t>(cdiv(M, kMaskRows), 65535)));
+    tg_relu_backward_vec_kernel<<<grid, 256, 0, st_>>>(
+        static_cast<const uint16_t*>(dC), lddc, static_cast<const uint16_t*>(C), ldc,
+        static_cast<uint16_t*>(dZ), lddz, M, N);
+  } else {
+    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(cdiv(N, 256), 32)),
+                    static_cast<unsigned>(std::min<int64_t>(M, 65535)));
+    tg_relu_backward_kernel<<<grid, 256, 0, st_>>>(
+        static_cast<const uint16_t*>(dC), lddc, static_cast<const uint16_t*>(C), ldc,
+        static_cast<uint16_t*>(dZ), lddz, M, N);
+  }
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? TG_OK : cuda_fail(e);
 }

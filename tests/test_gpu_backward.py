@@ -90,6 +90,31 @@ def test_relu_backward_kernel_bitwise():
     assert np.isnan(out[:, N:]).all()
 
 
+@pytest.mark.parametrize("M,N,ld", [(257, 259, 264), (256, 1024, 1024), (9, 5, 8), (1, 8, 8)])
+def test_relu_backward_vector_path_every_pattern(M, N, ld):
+    # 16-byte-aligned rows take the vectorised kernel (eight rows per thread, a tail thread for
+    # the last N mod 8 columns).  C holds every fp16 bit pattern in turn (NaNs, infinities,
+    # signed zeros, subnormals), so the mask is pinned bit for bit on that path too; the padding
+    # of dZ stays untouched.
+    pats = np.arange(M * N, dtype=np.int64) % 65536
+    C = np.zeros((M, ld), np.uint16)
+    C[:, :N] = pats.reshape(M, N).astype(np.uint16)
+    dC = np.zeros((M, ld), np.float16)
+    dC[:, :N] = inputs.tensor(M, N, 94, 0)
+    C_t = torch.from_numpy(C.view(np.float16)).cuda()
+    dC_t = torch.from_numpy(dC).cuda()
+    dZ = torch.full((M, ld + 8), float("nan"), dtype=torch.float16, device="cuda")
+    st = binding.tg_relu_backward_f16(dC_t.data_ptr(), C_t.data_ptr(), dZ.data_ptr(), M, N, ld,
+                                      ld, ld + 8, torch.cuda.current_stream().cuda_stream)
+    assert st == binding.TG_OK
+    torch.cuda.synchronize()
+    out = dZ.cpu().numpy()
+    want = oracle.relu_backward(np.ascontiguousarray(dC[:, :N]),
+                                np.ascontiguousarray(C[:, :N].view(np.float16)))
+    np.testing.assert_array_equal(out[:, :N].view(np.uint16), want)
+    assert np.isnan(out[:, N:]).all()
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 520, 777), (1024, 768, 2048)])
 def test_autograd_function(M, N, K):
     from fp16_gemm_relu_gb300.autograd import relu_matmul
