@@ -498,44 +498,77 @@ __global__ void tg_first_window_kernel(const uint16_t* __restrict__ A, int64_t l
 // residual).  W rows are ldw floats (multiple of 4, 16-byte aligned); C may have any 2-byte
 // alignment and leading dimension.  p supplies act, bias, residual, ldr, M and N.
 // With cls_rows > 0 the workspace rows are in class-major order (A read by row classes): row i
-// of C is workspace row (i mod 16) * cls_rows + i / 16.
-__global__ void tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ldw,
-                                        int64_t split_stride, int splits, __half* C,
-                                        int64_t ldc, const tg::GemmParams p,
-                                        int64_t cls_rows) {
+// of C is workspace row (i mod 16) * cls_rows + i / 16.  Thread g of the x range takes columns
+// 4g .. 4g + 3 of kReduceRows rows at a time, loading one split of all of them before adding
+// (a flat index split by a 64-bit division per item, one row at a time, ran at 0.67 of HBM).
+constexpr int kReduceRows = 4;
+constexpr int kReduceThreads = 128;
+__global__ void __launch_bounds__(kReduceThreads)
+    tg_splitk_reduce_kernel(const float* __restrict__ ws, int64_t ldw, int64_t split_stride,
+                            int splits, __half* C, int64_t ldc, const tg::GemmParams p,
+                            int64_t cls_rows) {
   const int64_t M = p.M, N = p.N;
-  const int64_t cpr = (N + 3) >> 2;
-  const int64_t total = M * cpr;
-  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
-       idx += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = idx / cpr;
-    const int64_t c0 = (idx - r * cpr) << 2;
-    const int64_t wr = cls_rows > 0 ? (r % tg::kARowClasses) * cls_rows + r / tg::kARowClasses : r;
-    const float* w = ws + wr * ldw + c0;
-    // splits == 0: the empty sum (K == 0 with a bias or residual epilogue)
-    float4 acc = splits > 0 ? __ldg(reinterpret_cast<const float4*>(w)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 1; s < splits; ++s) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(w + s * split_stride));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    float a[4] = {acc.x, acc.y, acc.z, acc.w};
-    __half h[4];
+  const int64_t g = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;  // group of 4 columns
+  if (g >= (N + 3) >> 2) return;
+  const int64_t c0 = g << 2;
+  for (int64_t r0 = int64_t(blockIdx.y) * kReduceRows; r0 < M;
+       r0 += int64_t(gridDim.y) * kReduceRows) {
+    // rows past M read row M - 1 (in bounds) and are never stored
+    const float* w[kReduceRows];
+    float4 acc[kReduceRows];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      h[e] = __float2half_rn(c0 + e < N ? tg::epilogue_value(a[e], int(r), int(c0 + e), p) : 0.0f);
-    __half* d = C + r * ldc + c0;
-    if (c0 + 4 <= N && (reinterpret_cast<uintptr_t>(d) & 7u) == 0) {
-      uint2 v;
-      v.x = uint32_t(__half_as_ushort(h[0])) | (uint32_t(__half_as_ushort(h[1])) << 16);
-      v.y = uint32_t(__half_as_ushort(h[2])) | (uint32_t(__half_as_ushort(h[3])) << 16);
-      *reinterpret_cast<uint2*>(d) = v;
-    } else {
-      for (int e = 0; e < 4 && c0 + e < N; ++e) d[e] = h[e];
+    for (int i = 0; i < kReduceRows; ++i) {
+      const int64_t r = r0 + i < M ? r0 + i : M - 1;
+      const int64_t wr =
+          cls_rows > 0 ? (r % tg::kARowClasses) * cls_rows + r / tg::kARowClasses : r;
+      w[i] = ws + wr * ldw + c0;
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);  // splits == 0: the empty sum (K == 0)
+    }
+    for (int s = 0; s < splits; ++s) {
+      float4 v[kReduceRows];
+#pragma unroll
+      for (int i = 0; i < kReduceRows; ++i)
+        v[i] = __ldg(reinterpret_cast<const float4*>(w[i] + s * split_stride));
+#pragma unroll
+      for (int i = 0; i < kReduceRows; ++i) {
+        if (s == 0) {
+          acc[i] = v[i];
+        } else {
+          acc[i].x += v[i].x;
+          acc[i].y += v[i].y;
+          acc[i].z += v[i].z;
+          acc[i].w += v[i].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kReduceRows; ++i) {
+      const int64_t r = r0 + i;
+      if (r >= M) break;
+      const float a[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+      __half h[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        h[e] = __float2half_rn(c0 + e < N ? tg::epilogue_value(a[e], int(r), int(c0 + e), p)
+                                          : 0.0f);
+      __half* d = C + r * ldc + c0;
+      if (c0 + 4 <= N && (reinterpret_cast<uintptr_t>(d) & 7u) == 0) {
+        uint2 v;
+        v.x = uint32_t(__half_as_ushort(h[0])) | (uint32_t(__half_as_ushort(h[1])) << 16);
+        v.y = uint32_t(__half_as_ushort(h[2])) | (uint32_t(__half_as_ushort(h[3])) << 16);
+        *reinterpret_cast<uint2*>(d) = v;
+      } else {
+        for (int e = 0; e < 4 && c0 + e < N; ++e) d[e] = h[e];
+      }
     }
   }
+}
+
+// Grid of the reduction: x over the groups of 4 columns, y over chunks of kReduceRows rows.
+dim3 reduce_grid(int64_t M, int64_t N) {
+  return dim3(static_cast<unsigned>(cdiv(cdiv(std::max<int64_t>(N, 1), 4), kReduceThreads)),
+              static_cast<unsigned>(std::min<int64_t>(cdiv(std::max<int64_t>(M, 1), kReduceRows),
+                                                      65535)));
 }
 
 // dZ[i, j] = C[i, j] > 0 ? dC[i, j] : +0 (the relu derivative taken on the forward output C;
@@ -686,7 +719,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     gp.ldr = epi.residual ? epi.ldr : 0;
     gp.M = static_cast<int>(M);
     gp.N = static_cast<int>(N);
-    tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
+    tg_splitk_reduce_kernel<<<reduce_grid(M, N), kReduceThreads, 0, stream>>>(
         nullptr, 0, 0, 0, static_cast<__half*>(C), ldc, gp, 0);
     e = cudaGetLastError();
     return e == cudaSuccess ? TG_OK : cuda_fail(e);
@@ -914,7 +947,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   }
 
   if (ws) {
-    tg_splitk_reduce_kernel<<<aux_grid(M * cdiv(N, 4), ds->sm_count), 256, 0, stream>>>(
+    tg_splitk_reduce_kernel<<<reduce_grid(M, N), kReduceThreads, 0, stream>>>(
         ws, pl.ldw, ws_rows * pl.ldw, P.split_k, static_cast<__half*>(C), ldc, reduce_params,
         P.a_row_classes ? pl.cls_rows : 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return fail(cuda_fail(e));
@@ -1018,7 +1051,7 @@ bool tensor_map_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) { return encode_f
 cudaError_t launch_splitk_reduce(const float* ws, int64_t ldw, int64_t split_stride, int splits,
                                  void* C, int64_t ldc, const GemmParams& p, int num_sms,
                                  cudaStream_t stream) {
-  tg_splitk_reduce_kernel<<<aux_grid(int64_t(p.M) * cdiv(p.N, 4), num_sms), 256, 0, stream>>>(
+  tg_splitk_reduce_kernel<<<reduce_grid(p.M, p.N), kReduceThreads, 0, stream>>>(
       ws, ldw, split_stride, splits, static_cast<__half*>(C), ldc, p, 0);
   return cudaGetLastError();
 }
