@@ -470,6 +470,68 @@ __global__ void tg_pack_rows_kernel(const uint16_t* __restrict__ src, int64_t ld
   }
 }
 
+// The same copy with each lane taking kPackItems chunks (of warp items nwarps apart) per pass,
+// all of their loads issued before its first store: for large copies, where every warp has
+// at least that many items (launch_pack).
+constexpr int kPackItems = 4;
+
+__global__ void tg_pack_rows4_kernel(const uint16_t* __restrict__ src, int64_t ld_src,
+                                     uint16_t* __restrict__ dst, int64_t ld_dst, int64_t rows,
+                                     int64_t cols) {
+  const int64_t cpr = (cols + 7) >> 3;
+  const int64_t gpr = (cpr + 31) >> 5;  // 32-chunk groups per row
+  const int64_t items = rows * gpr;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t it0 = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5; it0 < items;
+       it0 += kPackItems * nwarps) {
+    uint4 lo[kPackItems], hi[kPackItems];
+    uint32_t bs[kPackItems];
+    int nv[kPackItems];
+    int64_t out[kPackItems];  // element offset of the chunk in dst, or -1 when there is none
+#pragma unroll
+    for (int i = 0; i < kPackItems; ++i) {
+      const int64_t it = it0 + i * nwarps;
+      out[i] = -1;
+      if (it >= items) continue;
+      const int64_t r = it / gpr;
+      const int64_t c = ((it - r * gpr) << 5) + lane;
+      if (c >= cpr) continue;
+      const uintptr_t row = reinterpret_cast<uintptr_t>(src + r * ld_src);
+      const uint32_t b = static_cast<uint32_t>(row & 15u);
+      const uint4* blk = reinterpret_cast<const uint4*>(row - b) + c;
+      const int nvalid = static_cast<int>(cols - (c << 3) < 8 ? cols - (c << 3) : 8);
+      lo[i] = __ldg(blk);
+      hi[i] = (b + 2u * static_cast<uint32_t>(nvalid - 1) >= 16u) ? __ldg(blk + 1)
+                                                                 : make_uint4(0, 0, 0, 0);
+      bs[i] = b;
+      nv[i] = nvalid;
+      out[i] = r * ld_dst + (c << 3);
+    }
+#pragma unroll
+    for (int i = 0; i < kPackItems; ++i) {
+      if (out[i] < 0) continue;
+      const uint32_t b = bs[i];
+      const uint32_t w[8] = {lo[i].x, lo[i].y, lo[i].z, lo[i].w,
+                             hi[i].x, hi[i].y, hi[i].z, hi[i].w};
+      const uint32_t q = b >> 2;  // whole words to skip
+      uint32_t t[7], u[5];
+#pragma unroll
+      for (int k = 0; k < 7; ++k) t[k] = (q & 1u) ? w[k + 1] : w[k];
+#pragma unroll
+      for (int k = 0; k < 5; ++k) u[k] = (q & 2u) ? t[k + 2] : t[k];
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o[j] = (b & 2u) ? __funnelshift_r(u[j], u[j + 1], 16) : u[j];
+        if (2 * j >= nv[i]) o[j] = 0u;
+        else if (2 * j + 1 >= nv[i]) o[j] &= 0xFFFFu;
+      }
+      *reinterpret_cast<uint4*>(dst + out[i]) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // Element shifts of the 16 row classes of A (AClassMaps), passed by value.
 struct ClassShifts {
   int e[tg::kARowClasses];
@@ -648,6 +710,24 @@ int aux_grid(int64_t work_items, int num_sms, int per_sm = 8) {
   return static_cast<int>(std::min<int64_t>(blocks, int64_t(num_sms) * per_sm));
 }
 
+// One operand copy on `per_sm` blocks of 256 threads per SM at most.  For the copies made
+// before a single GEMM (`copies_first`), tg_pack_rows4_kernel takes kPackItems 32-chunk
+// items per pass, their loads together, when every warp has at least that many: 4096^3 with
+// odd strides ran 154 against 165 us per call (one process, one box).  Copies split by split
+// beside the GEMMs keep one item per pass: unrolled, 4095 x 3073 x 65537 measured 0-3% faster
+// depending on the box, and 300 x 1030 x 65537 2-4% slower.
+void launch_pack(const uint16_t* src, int64_t ld_src, uint16_t* dst, int64_t ld_dst,
+                 int64_t rows, int64_t cols, int num_sms, int per_sm, bool copies_first,
+                 cudaStream_t st) {
+  const int64_t cpr = cdiv(cols, 8);
+  const int grid = aux_grid(rows * cpr, num_sms, per_sm);
+  const int64_t items = rows * cdiv(cpr, 32);
+  if (copies_first && items >= kPackItems * int64_t(grid) * 8)
+    tg_pack_rows4_kernel<<<grid, 256, 0, st>>>(src, ld_src, dst, ld_dst, rows, cols);
+  else
+    tg_pack_rows_kernel<<<grid, 256, 0, st>>>(src, ld_src, dst, ld_dst, rows, cols);
+}
+
 // Blocks per SM of the operand copies that run beside the GEMM (overlapped copies).  On
 // 4095 x 3073 x 65537 (two runs each): 1 block 1.62 ms per step, 2: 1.43, 4: 1.32, 8: 1.33;
 // copies first, no overlap: 1.33-1.38.  With fewer blocks the copies themselves become the
@@ -754,26 +834,27 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
   uint16_t* Bp = P.repack_b ? reinterpret_cast<uint16_t*>(scratch + pl.off_b) : nullptr;
   // Copies of the K range [k0, k1) of A and B into their aligned scratch (A stored M x K:
   // columns k0..k1 of every row; stored K x M: rows k0..k1; B likewise).
-  auto copy_k_range = [&](int64_t k0, int64_t k1, cudaStream_t st, int per_sm) -> cudaError_t {
+  auto copy_k_range = [&](int64_t k0, int64_t k1, cudaStream_t st, int per_sm,
+                          bool copies_first) -> cudaError_t {
     const uint16_t* a16 = static_cast<const uint16_t*>(A);
     const uint16_t* b16 = static_cast<const uint16_t*>(B);
     if (P.repack_a) {
       if (ta)
-        tg_pack_rows_kernel<<<aux_grid((k1 - k0) * cdiv(M, 8), ds->sm_count, per_sm), 256, 0, st>>>(
-            a16 + k0 * lda, lda, Ap + k0 * pl.lda_p, pl.lda_p, k1 - k0, M);
+        launch_pack(a16 + k0 * lda, lda, Ap + k0 * pl.lda_p, pl.lda_p, k1 - k0, M, ds->sm_count,
+                    per_sm, copies_first, st);
       else
-        tg_pack_rows_kernel<<<aux_grid(M * cdiv(k1 - k0, 8), ds->sm_count, per_sm), 256, 0, st>>>(
-            a16 + k0, lda, Ap + k0, pl.lda_p, M, k1 - k0);
+        launch_pack(a16 + k0, lda, Ap + k0, pl.lda_p, M, k1 - k0, ds->sm_count, per_sm,
+                    copies_first, st);
       const cudaError_t ce = cudaGetLastError();
       if (ce != cudaSuccess) return ce;
     }
     if (P.repack_b) {
       if (tb)
-        tg_pack_rows_kernel<<<aux_grid(N * cdiv(k1 - k0, 8), ds->sm_count, per_sm), 256, 0, st>>>(
-            b16 + k0, ldb, Bp + k0, pl.ldb_p, N, k1 - k0);
+        launch_pack(b16 + k0, ldb, Bp + k0, pl.ldb_p, N, k1 - k0, ds->sm_count, per_sm,
+                    copies_first, st);
       else
-        tg_pack_rows_kernel<<<aux_grid((k1 - k0) * cdiv(N, 8), ds->sm_count, per_sm), 256, 0, st>>>(
-            b16 + k0 * ldb, ldb, Bp + k0 * pl.ldb_p, pl.ldb_p, k1 - k0, N);
+        launch_pack(b16 + k0 * ldb, ldb, Bp + k0 * pl.ldb_p, pl.ldb_p, k1 - k0, N, ds->sm_count,
+                    per_sm, copies_first, st);
       return cudaGetLastError();
     }
     return cudaSuccess;
@@ -795,7 +876,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
     overlap = cap == cudaStreamCaptureStatusNone;
   }
   if (!overlap && (P.repack_a || P.repack_b)) {
-    if ((e = copy_k_range(0, K, stream, 8)) != cudaSuccess) return fail(cuda_fail(e));
+    if ((e = copy_k_range(0, K, stream, 8, true)) != cudaSuccess) return fail(cuda_fail(e));
   }
 
   tg::GemmLaunch L;
@@ -921,7 +1002,7 @@ tg_status run_gemm(const void* A, const void* B, void* C, int64_t M, int64_t N, 
       const int64_t k0 = sp * kspan, k1 = std::min<int64_t>(K, k0 + kspan);
       cudaStream_t g = ov->gemm[sp & 1];
       // the first split's copy has the GPU to itself
-      ce = copy_k_range(k0, k1, ov->copy, sp == 0 ? 8 : kOverlapCopyBlocksPerSm);
+      ce = copy_k_range(k0, k1, ov->copy, sp == 0 ? 8 : kOverlapCopyBlocksPerSm, false);
       if (ce == cudaSuccess) ce = cudaEventRecord(ov->copied[sp], ov->copy);
       if (ce == cudaSuccess) ce = cudaStreamWaitEvent(g, ov->copied[sp], 0);
       if (ce != cudaSuccess) break;

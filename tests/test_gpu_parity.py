@@ -341,3 +341,26 @@ def test_cost_model_defaults_parity(M, N, K, lda, ldb, ldc, expect):
     bi = inputs.tensor(K, N, 98, 1, "int")
     ci, _ = run_gpu(ai, bi, True, None, lda=lda, ldb=ldb, ldc=ldc)
     np.testing.assert_array_equal(ci, oracle.gemm_relu(ai, bi, relu=True, want=("f32",))["out16_f32acc"])
+
+
+def test_large_unaligned_operands_copied_first():
+    # one K pass with both operands copied first: the copy takes four 32-chunk items per warp
+    # pass (all loads before the stores).  Odd leading dimensions and a 2-byte-aligned A.
+    M = N = K = 4096
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    st, plan = binding.tg_plan_query(0x100002, 0x200000, 0x300000, M, N, K, K + 3, N + 3, N + 1,
+                                     sms)
+    assert st == binding.TG_OK and plan["repack_a"] == 1 and plan["repack_b"] == 1
+    assert plan["split_k"] == 1 and plan["repack_overlap"] == 0, plan
+    a = inputs.tensor(M, K, 99, 0)
+    b = inputs.tensor(K, N, 99, 1)
+    c, pad_ok = run_gpu(a, b, True, None, lda=K + 3, ldb=N + 3, ldc=N + 1, a_off=1)
+    assert pad_ok
+    rows = np.array([0, 1, 7, 8, 2047, 4094, 4095])
+    assert_parity(c[rows], oracle.gemm_relu(a, b, relu=True, rows=rows), K, True,
+                  where="copies first, 4096^3")
+    ai = inputs.tensor(M, K, 100, 0, "int")
+    bi = inputs.tensor(K, N, 100, 1, "int")
+    ci, _ = run_gpu(ai, bi, True, None, lda=K + 3, ldb=N + 3, ldc=N + 1, a_off=1)
+    np.testing.assert_array_equal(
+        ci[rows], oracle.gemm_relu(ai, bi, relu=True, rows=rows, want=("f32",))["out16_f32acc"])
