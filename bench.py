@@ -33,7 +33,8 @@ from fp16_gemm_relu_gb300 import workloads  # noqa: E402
 METRIC = "GEMM+ReLU TFLOP/s (2MNK/t) and % of GB300 fp16 tensor/HBM roofline, 1 GPU"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DECODE_FIRST_MIN_M = 768  # the int4/NF4 GEMM's default: decode the weights first from this M
+# the int4 / NF4 GEMM's default: decode the weights first from this M
+DECODE_FIRST_MIN_M = {"w4": 512, "nf4": 384}
 FP16_OVER_BF16 = 1.0  # dense fp16 and bf16 tensor rates are equal (nominal 2.25 PF each)
 
 
@@ -49,7 +50,8 @@ def parse_args():
                          "(4MNK flops), all in the library's kernels")
     ap.add_argument("--dequant", default="none", choices=["none", "w4", "nf4"],
                     help="w4 / nf4: B is int4 / NF4 weights (group 128 scales), decoded inside "
-                         "the GEMM (or, for M >= 768, once into fp16 before the fp16 GEMM)")
+                         "the GEMM (or, for M >= 512 (int4) / 384 (NF4), once into fp16 before "
+                         "the fp16 GEMM)")
     ap.add_argument("--epilogue", default="relu", choices=["relu", "bias_gelu", "bias_relu_residual"],
                     help="relu: the metric's path; the others time the fused bias/GELU/residual "
                          "epilogue on the same GEMM")
@@ -475,9 +477,9 @@ def run_ours(args, wl):
         del B
         alg_bytes = 2 * wl.M * wl.K + wl.K * wl.N // 2 + 2 * wl.N * (-(-wl.K // G)) + 2 * wl.M * wl.N
         # the int4 plan the library picks for the two int4 workloads: the swapped-operand
-        # kernel for a few rows of A; for many (M >= 768, the library's default threshold)
+        # kernel for a few rows of A; for many (the library's default threshold per format)
         # the weights decoded once into fp16 scratch, then the fp16 GEMM
-        if wl.M >= DECODE_FIRST_MIN_M:
+        if wl.M >= DECODE_FIRST_MIN_M[args.dequant]:
             plan = {"block_m": 256, "block_n": 256, "block_k": 64, "kernels": 2,
                     "kernel": "tg_dequant_kernel (weights to fp16 scratch), then the fp16 GEMM"}
         elif wl.M <= 128:

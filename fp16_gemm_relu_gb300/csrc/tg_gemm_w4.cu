@@ -8,10 +8,15 @@
 
 namespace {
 
-// Smallest M for which the decode-first plan is chosen by default.  On GB300 (int4 / NF4,
-// L2 flushed): N = K = 8192 fused against decode-first at M = 512 92 / 104 us, M = 768
-// 166 / 142 us, M = 8192 1028 / 660 us; N = K = 4096 at M = 1024 51 / 47 us.
-constexpr int64_t kDecodeFirstMinM = 768;
+// Smallest M for which the decode-first plan is chosen by default, per weight format.  On
+// GB300 (L2 flushed, fused against decode-first, with the decode pass at 28.6 us for
+// 8192 x 8192): int4 at M = 256 65.6 / 78.8 us (N = K = 8192) and 180 / 214 us
+// (N = 28672); at M = 512 92.2 / 91.5, 38.2 / 38.5 (N = K = 4096), 254 / 249 (N = 28672) and
+// 287 / 258 (K = 28672); at M = 640 166 / 114.  NF4, whose fused decode costs more: at
+// M = 384 97.4 / 91.8; at M = 256 79.9 / 79.6, 45.1 / 37.0 (N = K = 4096) and 193 / 218
+// (N = 28672).
+constexpr int64_t kDecodeFirstMinMInt4 = 512;
+constexpr int64_t kDecodeFirstMinMNf4 = 384;
 
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -162,7 +167,8 @@ tg_status run_dequant(const void* A, const void* Wq, const void* scales, void* C
   // as fp16 (K x N x 2 bytes) costs less than decoding every weight tile inside the GEMM.
   const bool fused_override = o.swap_ab != 0 || o.pair != 0 || o.block_n != 0 ||
                               o.tmem_decode != 0;
-  if (o.dequant_first > 0 || (o.dequant_first == 0 && !fused_override && M >= kDecodeFirstMinM)) {
+  const int64_t min_m = FMT == tg::kFmtInt4 ? kDecodeFirstMinMInt4 : kDecodeFirstMinMNf4;
+  if (o.dequant_first > 0 || (o.dequant_first == 0 && !fused_override && M >= min_m)) {
     const int64_t ldw = (N + 7) / 8 * 8;
     void* w16 = nullptr;
     st = tg::scratch_alloc(size_t(K) * size_t(ldw) * 2, stream, &w16);

@@ -212,9 +212,10 @@ tg_status tg_relu_backward_f16(const void* dC, const void* C, void* dZ, int64_t 
  * scales: device fp16, ceil(K/G) rows of lds values (lds >= N, multiple of 8, 16-byte
  *     aligned).  group_size G: a multiple of 64.
  * C: device fp16 M x N, 16-byte aligned, ldc a multiple of 8.  epi as tg_gemm_f16_epilogue.
- * Plans: by default for M >= 768 with no int4-kernel override (opt->dequant_first), the whole
- * weight matrix is decoded once into fp16 scratch from the library's pool (K x N rounded up to
- * 8, 2 bytes each; released in stream order), the same values the fused kernels use, and the
+ * Plans: by default for M >= 512 (int4; NF4: M >= 384) with no int4-kernel override
+ * (opt->dequant_first), the whole weight matrix is decoded once into fp16 scratch from the
+ * library's pool (K x N rounded up to 8, 2 bytes each; released in stream order), the same
+ * values the fused kernels use, and the
  * fp16 GEMM (tg_gemm_f16_epilogue) runs on it; without scratch the plan falls back to a fused
  * kernel (TG_ERR_NO_WORKSPACE only when dequant_first = 1 forces it).  Otherwise the weights are
  * decoded inside the GEMM kernel (never written to memory).  Fused kernels: for

@@ -162,7 +162,7 @@ def test_decode_first(fmt, M, N, K, G, act):
 
 @pytest.mark.parametrize("fmt", ["int4", "nf4"])
 def test_decode_first_is_the_default_for_large_m(fmt):
-    # with no kernel override, M >= 768 takes the decode-first plan: bitwise what forcing it
+    # with no kernel override, a large M takes the decode-first plan: bitwise what forcing it
     # gives (each plan is deterministic)
     M, N, K, G = 1024, 768, 2048, 128
     a, Wq, S = make(M, N, K, G, 43)
@@ -172,6 +172,20 @@ def test_decode_first_is_the_default_for_large_m(fmt):
     check(auto, a, Wq, S, N, G, "relu", fmt=fmt)
     fused = run_w4(a, Wq, S, N, G, act=1, options={"dequant_first": -1}, fmt=fmt)
     check(fused, a, Wq, S, N, G, "relu", fmt=fmt)
+
+
+@pytest.mark.parametrize("fmt,M,first", [("int4", 511, False), ("int4", 512, True),
+                                          ("nf4", 383, False), ("nf4", 384, True)])
+def test_decode_first_threshold(fmt, M, first):
+    # the default switches to decode-first at M = 512 for int4 and M = 384 for NF4 weights
+    # (NF4's fused decode costs more): bitwise what forcing that plan gives, and the oracle's
+    N, K, G = 520, 1030, 128
+    a, Wq, S = make(M, N, K, G, 44)
+    auto = run_w4(a, Wq, S, N, G, act=1, fmt=fmt)
+    forced = run_w4(a, Wq, S, N, G, act=1, options={"dequant_first": 1 if first else -1},
+                    fmt=fmt)
+    np.testing.assert_array_equal(auto, forced)
+    check(auto, a, Wq, S, N, G, "relu", fmt=fmt)
 
 
 @pytest.mark.parametrize("act", ["relu", "gelu_tanh"])
