@@ -57,7 +57,8 @@ def parse_args():
                          "epilogue on the same GEMM")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-workloads", action="store_true",
-                    help="skip timing the other named workloads (the 'workloads' block)")
+                    help="skip timing the other named workloads and the backward, epilogue and "
+                         "int4/NF4 variants (the 'workloads' and 'variants' blocks)")
     ap.add_argument("--workload-seconds", type=float, default=0.5,
                     help="minimum wall time of each other workload's timed region")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -433,6 +434,131 @@ def other_workloads(args, headline, lib, binding, dev, stream, bus, peaks, peak_
     return out
 
 
+def other_variants(args, lib, binding, dev, stream, bus, peaks, peak_src, A, B):
+    """The scope table's further rows, each timed like the workloads block (W warm-up steps,
+    CUDA events per step, L2 flushed between steps when the operands fit in it, at least
+    `args.workload_seconds` of steps): the backward step and the two fused epilogues on
+    8192^3 (A and B are the headline's operands), and the int4 / NF4 weight GEMMs on 8192^3
+    and on 64 x 28672 x 8192.  A variant that fails records its error instead of a time."""
+    import torch
+
+    from fp16_gemm_relu_gb300 import inputs as _inputs
+
+    handle = stream.cuda_stream
+    sq = workloads.get("square8192")
+    sk = workloads.get("skinny64x28672x8192")
+
+    def check(st, what):
+        if st != 0:
+            raise binding.TgError(st, what)
+
+    def backward():
+        C = torch.empty((sq.M, sq.N), dtype=torch.float16, device=dev)
+        check(lib.tg_gemm_relu_f16(A.data_ptr(), B.data_ptr(), C.data_ptr(), sq.M, sq.N, sq.K,
+                                   sq.K, sq.N, sq.N, binding.TG_EPILOGUE_RELU, handle), "forward")
+        dC = torch.from_numpy(_inputs.tensor(sq.M, sq.N, sq.seed + 102, 1)).to(dev)
+        dZ, dA, dB = torch.empty_like(dC), torch.empty_like(A), torch.empty_like(B)
+
+        def step():
+            st = lib.tg_relu_backward_f16(dC.data_ptr(), C.data_ptr(), dZ.data_ptr(), sq.M, sq.N,
+                                          sq.N, sq.N, sq.N, handle)
+            if st == 0:
+                st = lib.tg_gemm_f16_t(0, 1, dZ.data_ptr(), B.data_ptr(), dA.data_ptr(), sq.M,
+                                       sq.K, sq.N, sq.N, sq.N, sq.K, None, None, handle)
+            if st == 0:
+                st = lib.tg_gemm_f16_t(1, 0, A.data_ptr(), dZ.data_ptr(), dB.data_ptr(), sq.K,
+                                       sq.N, sq.M, sq.K, sq.N, sq.N, None, None, handle)
+            check(st, "backward step")
+        return step, sq, 2 * sq.flops, sq.algorithmic_bytes, 3, (C, dC, dZ, dA, dB)
+
+    def epilogue(kind):
+        def make():
+            C = torch.empty((sq.M, sq.N), dtype=torch.float16, device=dev)
+            bias = torch.from_numpy(_inputs.tensor(1, sq.N, sq.seed + 100, 0).ravel()).to(dev)
+            resid = None
+            act = binding.TG_ACT_GELU
+            if kind == "bias_relu_residual":
+                resid = torch.from_numpy(_inputs.tensor(sq.M, sq.N, sq.seed + 101, 1)).to(dev)
+                act = binding.TG_ACT_RELU
+            epi = binding.tg_epilogue(act, bias.data_ptr(),
+                                      resid.data_ptr() if resid is not None else None,
+                                      sq.N if resid is not None else 0)
+
+            def step():
+                check(lib.tg_gemm_f16_epilogue(A.data_ptr(), B.data_ptr(), C.data_ptr(), sq.M,
+                                               sq.N, sq.K, sq.K, sq.N, sq.N, ctypes.byref(epi),
+                                               None, handle), "tg_gemm_f16_epilogue")
+            return step, sq, sq.flops, sq.algorithmic_bytes, 1, (C, bias, resid, epi)
+        return make
+
+    def weights(w, fmt):
+        def make():
+            G = 128
+            Aw = A if w is sq else torch.from_numpy(w.make_a()).to(dev)
+            ldq = -(-(-(-w.N // 8)) // 4) * 4
+            Wq = torch.from_numpy(_inputs.int4_weights(w.K, w.N, w.seed, ldq=ldq)
+                                  .view(np.int32)).to(dev)
+            Sc = torch.from_numpy(_inputs.int4_scales(-(-w.K // G), w.N, w.seed,
+                                                      1.0 / np.sqrt(w.K))).to(dev)
+            C = torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+            fn = lib.tg_gemm_w4a16_f16 if fmt == "w4" else lib.tg_gemm_nf4a16_f16
+            alg = 2 * w.M * w.K + w.K * w.N // 2 + 2 * w.N * (-(-w.K // G)) + 2 * w.M * w.N
+            kernels = 2 if w.M >= DECODE_FIRST_MIN_M[fmt] else 1
+
+            def step():
+                check(fn(Aw.data_ptr(), Wq.data_ptr(), Sc.data_ptr(), C.data_ptr(), w.M, w.N, w.K,
+                         w.K, ldq, w.N, w.N, G, None, None, handle), f"{fmt} GEMM")
+            return step, w, w.flops, alg, kernels, (Aw, Wq, Sc, C)
+        return make
+
+    variants = [("square8192/backward", backward),
+                ("square8192/bias_gelu", epilogue("bias_gelu")),
+                ("square8192/bias_relu_residual", epilogue("bias_relu_residual")),
+                ("square8192/w4", weights(sq, "w4")), ("square8192/nf4", weights(sq, "nf4")),
+                ("skinny64x28672x8192/w4", weights(sk, "w4")),
+                ("skinny64x28672x8192/nf4", weights(sk, "nf4"))]
+    out = {}
+    for name, make in variants:
+        try:
+            step, w, flops_step, alg, kernels, keep = make()
+            in_bytes = alg - 2 * w.M * w.N
+            scrub = (torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+                     if in_bytes <= L2_BYTES else None)
+            with torch.cuda.stream(stream):
+                for _ in range(max(args.warmup, 3)):
+                    if scrub is not None:
+                        scrub.fill_(1.0)
+                    step()
+                _, probe_ms = timed_steps(torch, step, stream, 3, scrub)
+                steps = int(min(max(args.steps, args.workload_seconds * 1e3 /
+                                    max(probe_ms / 3, 1e-3)), 100000))
+                sampler = ClockSampler(bus)
+                step_ms, region_ms = timed_steps(torch, step, stream, steps, scrub, sampler)
+            st, word = binding.tg_device_error_check(clear=True)
+            if st != 0:
+                raise RuntimeError(f"device error word {word:#x}")
+            ms = statistics.mean(step_ms)
+            roof = roofline(w.flops, alg, flops_step, ms, peaks, peak_src)
+            rl = {k: roof[k] for k in ("bound", "achieved", "unit", "peak", "frac")}
+            if roof["bound"] == "tensor" and "bf16_tflops_sustained" in peaks:
+                # about half a second of back-to-back steps: the power-capped regime of the
+                # sustained peak
+                rl["peak_sustained"] = peaks["bf16_tflops_sustained"] * FP16_OVER_BF16
+                rl["frac_of_sustained"] = roof["achieved"] / rl["peak_sustained"]
+            out[name] = {"M": w.M, "N": w.N, "K": w.K, "steps": steps, "ms_per_step": ms,
+                         "value": flops_step / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                         "roofline": rl,
+                         "step_kernels": kernels,
+                         "l2": "flushed between steps" if scrub is not None
+                               else "operands larger than L2",
+                         "clocks": sampler.summary(), "region_ms": region_ms}
+            del keep, scrub
+        except Exception as e:  # recorded in the line; the other variants still run
+            out[name] = {"error": f"{type(e).__name__}: {e}"}
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, wl):
     import torch
 
@@ -627,6 +753,9 @@ def run_ours(args, wl):
             and args.epilogue == "relu" and args.dequant == "none"):
         line["workloads"] = other_workloads(args, wl.name, lib, binding, dev, stream, bus, peaks,
                                             peak_src)
+        if wl.name == "square8192":
+            line["variants"] = other_variants(args, lib, binding, dev, stream, bus, peaks,
+                                              peak_src, A, B)
 
     if rank == 0 and not args.no_e2e and args.pass_ == "forward" and args.dequant == "none":
         line["e2e"] = e2e(wl, A_h, B_h, dev, max(3, min(args.steps, 10)))
